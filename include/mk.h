@@ -1,0 +1,219 @@
+/*
+ * mk.h -- C ABI of the GB300 persistent verify-step megakernel.
+ *
+ * One call runs ONE speculative-verify decode step of a mixture-of-experts
+ * transformer for a block of T = k+1 tokens (the last accepted token followed by
+ * k drafts), fused into a single persistent kernel launch.
+ *
+ * What the call computes comes from two pages:
+ *  - "Why one GB300 doesn't beat 4x RTX PRO 6000 at single-stream decode"
+ *    (al-engr), section "The decomposition": tokens/s = tokens per verify step x
+ *    verify steps/s, with tokens per step = accepted drafts + 1; section "Where the
+ *    11.2 ms goes": the step is a stack of 43 MoE layers with 384 experts, decode
+ *    attention, dense projections, a router top-k, an lm_head and one accept
+ *    (rejection) kernel per step, spread over ~1,300 small kernels that this
+ *    library replaces with one launch.
+ *  - "DeepSeek-V4.1-Flash breaks 1,000 tokens per second for one user" (ezolabs),
+ *    sections "How we got here" and "Serving stack": drafted tokens are checked
+ *    together in blocks (block verification), 5-token draft blocks; the plugin
+ *    keeps one persistent block per SM and refuses configurations it cannot run
+ *    ("no silent fallback", section "What NVIDIA shipped").
+ * The per-layer equations (pre-norm GQA attention with rotate-half RoPE over a
+ * paged KV cache, sigmoid router with selection-only bias and top-K weights
+ * normalised to 1, SwiGLU routed experts plus one shared expert) are the plain
+ * reading of the workload the pages describe; the same reading drives the fp64
+ * oracle in oracle/.
+ *
+ * Conventions for every entry point
+ *  - All tensors are row-major and owned by the caller; the library never copies
+ *    or frees them.  "dev" pointers are CUDA device memory on the current device,
+ *    "host" pointers are host memory.  The library owns only its workspace
+ *    (allocated in mk_create, freed in mk_destroy).
+ *  - Calls taking a stream are asynchronous on that stream (a cudaStream_t passed
+ *    as void*, NULL = legacy default stream).  Errors that the host can see are
+ *    returned at once and nothing is launched; errors found on the device (a bad
+ *    position or page-table entry, a wait that ran past its time limit) are
+ *    recorded in a device status word that mk_get_status reads.  After a device
+ *    error every later step exits at once until mk_reset is called.
+ *  - A state is not thread-safe and allows one step in flight at a time.
+ *  - There is no fallback path: unsupported shapes, dtypes or devices return
+ *    MK_ERR_UNSUPPORTED.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MK_OK = 0,
+    MK_ERR_INVALID = -1,      /* bad argument (null pointer, T out of range, ...)      */
+    MK_ERR_UNSUPPORTED = -2,  /* shape/dtype/device this build does not run           */
+    MK_ERR_NOMEM = -3,        /* workspace allocation failed                           */
+    MK_ERR_TIMEOUT = -4,      /* a device-side wait ran past timeout_ms                */
+    MK_ERR_CUDA = -5,         /* a CUDA runtime call failed                            */
+    MK_ERR_BAD_STATE = -6,    /* call not valid in the current state                   */
+    MK_ERR_BAD_INPUT = -7     /* device-side input check failed (positions, page table)*/
+} mk_status;
+
+/* storage types of weights and of the KV cache */
+enum {
+    MK_DT_F32 = 0,           /* float32                                                 */
+    MK_DT_BF16 = 1,          /* bfloat16                                                */
+    MK_DT_FP8E4M3_B128 = 2   /* FP8 E4M3 codes + float32 scale per 1x128 input block:   */
+                             /* W[n][k] = fp8(q[n][k]) * scale[k/128][n]                */
+};
+
+#define MK_DESC_VERSION 1
+
+/* Model description.  Limits of this build: T <= 8; hidden, expert_inter and
+ * n_q_heads*head_dim multiples of 128 and <= 4096; head_dim 64 or 128;
+ * page_size 64; (n_q_heads/n_kv_heads)*T <= 64; n_experts <= 512; top_k <= 8;
+ * n_shared 0 or 1; F32 weights only with hidden <= 2048 and an all-F32 model. */
+typedef struct {
+    int version;              /* MK_DESC_VERSION                                      */
+    int n_layers, hidden, n_q_heads, n_kv_heads, head_dim;
+    float rope_base, rms_eps;
+    int n_experts, top_k, n_shared, expert_inter;
+    int vocab;                /* 0: no embedding / LM head (mk_layer_forward only)    */
+    int page_size;            /* KV positions per page                                */
+    int max_T;                /* largest verify block that will be passed (<= 8)      */
+    int max_pages_per_stream; /* page-table row length; bounds positions              */
+    int weight_dtype;         /* MK_DT_* of attention and expert matrices             */
+    int router_dtype;         /* MK_DT_F32 or MK_DT_BF16                              */
+    int kv_dtype;             /* MK_DT_F32 or MK_DT_BF16                              */
+    int timeout_ms;           /* limit of every device-side wait; 0 means 1000 ms     */
+} mk_model_desc;
+
+/* One layer's weights (dev pointers).  Shapes, with d = head_dim, H = hidden,
+ * E = n_experts, I = expert_inter, NQKV = (n_q_heads + 2*n_kv_heads)*d:
+ *   attn_norm, moe_norm  float32 [H]
+ *   w_qkv   [NQKV][H]  rows: n_q_heads q heads, then n_kv_heads k heads, then v heads
+ *   w_o     [H][n_q_heads*d]
+ *   w_router [E][H] in router_dtype;  router_bias float32 [E] (selection only)
+ *   w1, w3  [E][I][H];  w2 [E][H][I]        routed experts (gate, up, down)
+ *   ws1, ws3 [I][H];    ws2 [H][I]          shared expert (NULL when n_shared = 0)
+ * FP8 matrices carry a float32 scale array laid out [in/128][out] (for the
+ * expert stacks [E][in/128][out]); it is ignored for other dtypes. */
+typedef struct {
+    const float *attn_norm;
+    const void *w_qkv;  const float *w_qkv_scale;
+    const void *w_o;    const float *w_o_scale;
+    const float *moe_norm;
+    const void *w_router;
+    const float *router_bias;
+    const void *w1;     const float *w1_scale;
+    const void *w3;     const float *w3_scale;
+    const void *w2;     const float *w2_scale;
+    const void *ws1;    const float *ws1_scale;
+    const void *ws3;    const float *ws3_scale;
+    const void *ws2;    const float *ws2_scale;
+} mk_layer_weights;
+
+typedef struct {
+    const void *embed;               /* bf16 [vocab][H] (dev; NULL if vocab == 0)     */
+    const float *final_norm;         /* float32 [H]                                   */
+    const void *lm_head;             /* bf16 [vocab][H]                               */
+    const mk_layer_weights *layers;  /* HOST array of n_layers entries                */
+} mk_weights;
+
+/* Paged KV cache.  Layer l keeps k_pool[l], v_pool[l] (dev), each
+ * [n_pages][n_kv_heads][page_size][head_dim] in kv_dtype; entries are stored
+ * already rotated.  page_table (dev int32 [n_streams][max_pages_per_stream])
+ * maps logical page j of a stream (positions j*P .. j*P+P-1) to a physical
+ * page.  A step with positions p_t = ctx + t reads positions < ctx and writes
+ * K/V of its T tokens at positions ctx..ctx+T-1; the caller then advances ctx
+ * by accepted + 1 (rejected slots are overwritten by the next step). */
+typedef struct {
+    void *const *k_pool;             /* HOST array [n_layers] of dev pointers         */
+    void *const *v_pool;
+    const int32_t *page_table;       /* dev                                           */
+    int n_pages;                     /* physical pages in each pool                   */
+} mk_kv_cache;
+
+typedef struct {
+    uint64_t steps;                  /* completed verify steps since create/reset     */
+    uint64_t accepted_sum;           /* sum of accepted draft counts                   */
+    uint64_t distinct_experts_sum;   /* routed experts streamed, summed over layers    */
+    int32_t last_accepted;
+    int32_t last_distinct_experts;   /* summed over the layers of the last step        */
+    int32_t fused;                   /* 1: the persistent fused kernel ran             */
+    int32_t grid_ctas;               /* persistent CTAs (one per SM)                   */
+    int32_t launches_per_step;       /* kernel launches per step (1)                   */
+    int32_t barriers_per_step;       /* grid-wide barriers per step                    */
+} mk_stats;
+
+typedef struct mk_state mk_state;
+
+/* Validate the description, check the device (compute capability 10.3, all
+ * persistent CTAs co-resident), build TMA descriptors for every weight matrix,
+ * precompute the RoPE table (fp64 on the host, stored fp32) and allocate the
+ * workspace.  Weights must stay valid until mk_destroy.  On success *out owns
+ * the state.  Errors: MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_NOMEM, MK_ERR_CUDA. */
+mk_status mk_create(const mk_model_desc *desc, const mk_weights *weights, mk_state **out);
+
+/* One verify step for one stream.
+ *   draft_tokens  dev int32 [T]: d_0 (last accepted token) then the k drafts
+ *   positions     dev int32 [T]: must be ctx, ctx+1, ..., ctx+T-1
+ *   kv            cache (its page table row 0 is used)
+ *   out_logits    dev float32 [T][vocab]
+ *   out_accepted  dev int32 [1]: n = longest prefix of drafts with d_i = argmax_{i-1}
+ *   out_argmax    dev int32 [T] or NULL
+ * Requires vocab > 0 and 1 <= T <= max_T. */
+mk_status mk_decode_step(mk_state *st, const int32_t *draft_tokens, int T,
+                         const int32_t *positions, const mk_kv_cache *kv,
+                         float *out_logits, int32_t *out_accepted, int32_t *out_argmax,
+                         void *stream);
+
+/* The same step through HOST buffers: copies the tokens and positions in, runs
+ * the step, copies the results out and synchronizes the stream.  out_logits and
+ * out_argmax may be NULL.  Returns the device status of the step. */
+mk_status mk_decode_step_host(mk_state *st, const int32_t *h_tokens, int T,
+                              const int32_t *h_positions, const mk_kv_cache *kv,
+                              float *h_logits, int32_t *h_accepted, int32_t *h_argmax,
+                              void *stream);
+
+/* One decoder layer on a given hidden state (no embedding, LM head or accept).
+ *   hidden_in, hidden_out  dev float32 [T][H] (may not alias)
+ *   out_topk_idx           dev int32 [T][top_k] or NULL (selected experts, key order)
+ *   out_topk_w             dev float32 [T][top_k] or NULL (their weights)
+ * K/V of the T tokens are written into layer `layer` of the cache. */
+mk_status mk_layer_forward(mk_state *st, int layer, const float *hidden_in, int T,
+                           const int32_t *positions, const mk_kv_cache *kv,
+                           float *hidden_out, int32_t *out_topk_idx, float *out_topk_w,
+                           void *stream);
+
+/* Record, on every later mk_decode_step, each layer's selected experts into
+ * trace (dev int32 [n_layers][T][top_k], key order); NULL turns it off.  The
+ * buffer must stay valid while tracing is on.  Used to check routing layer by
+ * layer against a reference. */
+mk_status mk_set_routing_trace(mk_state *st, int32_t *trace);
+
+/* Synchronize the last stream used and return the device status of the last
+ * step (MK_OK, MK_ERR_TIMEOUT or MK_ERR_BAD_INPUT). */
+mk_status mk_get_status(mk_state *st);
+
+/* Synchronize and copy the counters. */
+mk_status mk_get_stats(mk_state *st, mk_stats *out);
+
+/* Clear the device status, barrier epochs and counters (synchronous). */
+mk_status mk_reset(mk_state *st);
+
+/* Free the workspace.  Safe on NULL. */
+void mk_destroy(mk_state *st);
+
+/* Static text for a status code. */
+const char *mk_status_string(mk_status s);
+
+/* Text of the last host-side error of this state (a buffer inside the state);
+ * with st == NULL, the reason the calling thread's last mk_create failed. */
+const char *mk_last_error(const mk_state *st);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

@@ -1,0 +1,117 @@
+// Internal layout shared by the host API (mk_api.cu) and the persistent kernel
+// (mk_kernel.cu).  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mk.h"
+
+// ---- build-time limits -----------------------------------------------------
+#define MK_NCWARPS 8                     // consumer (compute) warps per CTA
+#define MK_THREADS ((MK_NCWARPS + 1) * 32) // + one producer (TMA) warp
+#define MK_RING 8                        // shared-memory ring slots
+#define MK_SLOT 16384                    // bytes per slot: one 128-row x 128-byte TMA box
+#define MK_MAXT 8                        // tokens per verify block (one N=8 MMA tile)
+#define MK_MAXKB 32                      // 128-column blocks of the widest GEMV input (4096)
+#define MK_MAXE 512                      // routed experts
+#define MK_MAXK 8                        // top-k
+#define MK_MAXD (MK_MAXT * MK_MAXK)      // distinct experts per layer
+#define MK_MAXROWS 64                    // (q heads per kv head) x T
+#define MK_MAXSPLIT 160                  // attention splits per kv head
+#define MK_FX 4294967296.0f              // fixed-point scale of the cross-CTA accumulators
+
+// Dynamic shared memory map (bytes).
+#define SM_RING 0
+#define SM_SCALE (SM_RING + MK_RING * MK_SLOT)
+#define SM_SCRATCH (SM_SCALE + MK_RING * 512)
+#define SM_SCRATCH_BYTES 65536
+#define SM_ROUTE (SM_SCRATCH + SM_SCRATCH_BYTES)
+#define SM_ROUTE_BYTES 4096
+#define SM_BAR (SM_ROUTE + SM_ROUTE_BYTES)
+#define SM_MISC (SM_BAR + 256)
+#define SM_TOTAL (SM_MISC + 256)
+
+// stages of one layer, in stream order
+enum { ST_QKV = 0, ST_ATT, ST_O, ST_ROUTER, ST_SHA, ST_EXPA, ST_EXPB, ST_LM };
+
+// one weight matrix, or a stack of E expert matrices, streamed by TMA
+struct DMat {
+    const CUtensorMap *tmap;   // 64-byte aligned descriptor in device memory
+    const float *scale;        // FP8: [E][cols/128][rows]
+    int dtype;                 // MK_DT_*
+    int rows, cols;            // per expert
+    int n_rg;                  // 128-row groups
+    int n_kc;                  // 128-byte column chunks
+    int is3d;                  // expert stack
+    int es;                    // element size (bytes)
+    long long scale_estride;   // floats per expert in `scale`
+};
+
+struct DLayer {
+    const float *attn_norm, *moe_norm, *router_bias;
+    DMat qkv, o, router, w1, w3, w2, s1, s3, s2;
+};
+
+// control block in device memory
+struct Ctrl {
+    unsigned long long bar_count;      // monotonic grid-barrier arrivals
+    unsigned long long epoch;          // bar_count at the start of the next launch
+    int abort;                         // set by the first failing wait
+    int status;                        // first device error (mk_status)
+    int where;                         // diagnostic code of the failing wait
+    int pad0;
+    unsigned long long steps, accepted_sum, distinct_sum;
+    int last_accepted, last_distinct;
+};
+
+struct DModel {
+    int L, H, Hq, Hkv, d, E, K, I, V, P, nshared, max_pages, maxT, G;
+    int wdt, rdt, kvdt, kv_es, nqkv;
+    float eps;
+    long long timeout_ns;
+    const DLayer *layers;              // [L]
+    const uint16_t *embed;             // bf16 [V][H]
+    const float *final_norm;
+    DMat lm;
+    const float2 *rope;                // [max_pages*P][d/2] (cos, sin)
+    // workspace
+    Ctrl *ctrl;
+    int *att_cnt;                      // [L][Hkv]
+    long long *qkv_acc;                // [MAXT][nqkv]
+    long long *res;                    // [MAXT][H]   residual stream
+    long long *rlog;                   // [MAXT][E]   router logits (un-normalised)
+    long long *sh_acc;                 // [MAXT][2][I] shared expert gate/up
+    long long *ea_acc;                 // [MAXT][K][2][I] routed expert gate/up
+    long long *logit_acc;              // [MAXT][V]
+    float *ssq;                        // [3][MAXKB][MAXT] sum-of-squares partials
+    float *o_buf;                      // [MAXT][Hq*d] attention output
+    float *att_part;                   // [Hkv][MAXSPLIT][MAXROWS][d+2]
+    float *cand_v;                     // [G][MAXT] argmax candidates
+    int *cand_i;
+};
+
+struct Params {
+    const DModel *m;
+    const CUtensorMap *kvmaps;         // [L][2] (K, V)
+    void *const *kpool;                // dev array [L]
+    void *const *vpool;
+    const int32_t *page_table;
+    const int32_t *tokens;
+    const int32_t *positions;
+    int T;
+    int mode;                          // 0: full step, 1: one layer
+    int layer;                         // mode 1
+    int n_pages;
+    float *out_logits;
+    int32_t *out_accepted;
+    int32_t *out_argmax;
+    const float *hidden_in;
+    float *hidden_out;
+    int32_t *out_idx;
+    float *out_w;
+    int32_t *trace;                    // [L][T][K] routing trace or null
+};
+
+cudaError_t mk_launch(const Params &p, int grid, size_t smem, cudaStream_t s);
+cudaError_t mk_kernel_setup(size_t smem);

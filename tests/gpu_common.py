@@ -1,0 +1,116 @@
+"""Shared pieces of the GPU parity tests: run the C-ABI path, run the oracle on
+the same seeded inputs, compare by the rules of the verify-step contract."""
+import numpy as np
+import torch
+
+import oracle
+from latency_moe_decode_persistent_gb300 import mk, synth
+from tests import helpers
+
+GAP = 1e-3            # decisive routing / argmax gap
+TOL = {synth.WDT_F32: 1e-4, synth.WDT_BF16: 2e-2, synth.WDT_FP8: 6e-2}
+
+
+class Built:
+    """A model + KV cache on the GPU and a library state bound to them."""
+
+    def __init__(self, cfg, ctxs=None, T=None, max_T=None, device="cuda", timeout_ms=0):
+        self.cfg = cfg
+        self.model = synth.make_model(cfg, device)
+        self.kv = synth.make_kv(cfg, device, ctxs=ctxs, T=T if T is not None else cfg.T)
+        self.max_T = max_T or max(cfg.T, T or 0)
+        self.args = mk.ModelArgs(self.model, self.max_T, self.kv.max_pages, timeout_ms)
+        self.st = mk.mk_create(self.args.desc, self.args.weights)
+        self.kvargs = mk.KVArgs(self.kv.k_pools, self.kv.v_pools, self.kv.page_table,
+                                self.kv.n_pages)
+
+    def close(self):
+        mk.mk_destroy(self.st)
+        self.st = None
+
+    def positions(self, T, stream=0):
+        c = self.kv.ctx[stream]
+        return torch.arange(c, c + T, dtype=torch.int32, device="cuda")
+
+    def layer(self, x, l=0, T=None):
+        T = x.shape[0] if T is None else T
+        out = torch.empty_like(x)
+        K = self.cfg.top_k
+        idx = torch.full((T, K), -1, dtype=torch.int32, device="cuda")
+        w = torch.zeros((T, K), dtype=torch.float32, device="cuda")
+        mk.mk_layer_forward(self.st, l, x, T, self.positions(T), self.kvargs.kv, out, idx, w)
+        st = mk.mk_get_status(self.st)
+        assert st == mk.MK_OK, mk.mk_last_error(self.st)
+        return out, idx, w
+
+    def step(self, tokens, trace=True):
+        T = len(tokens)
+        tok = torch.tensor(tokens, dtype=torch.int32, device="cuda")
+        logits = torch.empty((T, self.cfg.vocab), dtype=torch.float32, device="cuda")
+        acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+        am = torch.empty(T, dtype=torch.int32, device="cuda")
+        tr = None
+        if trace:
+            tr = torch.full((self.cfg.n_layers, T, self.cfg.top_k), -1, dtype=torch.int32,
+                            device="cuda")
+            mk.mk_set_routing_trace(self.st, tr)
+        mk.mk_decode_step(self.st, tok, T, self.positions(T), self.kvargs.kv, logits, acc, am)
+        st = mk.mk_get_status(self.st)
+        assert st == mk.MK_OK, mk.mk_last_error(self.st)
+        if trace:
+            mk.mk_set_routing_trace(self.st, None)
+        return logits, int(acc.item()), am, tr
+
+
+def kth_gap(key_row, K):
+    s = np.sort(key_row)[::-1]
+    return s[K - 1] - s[K] if len(s) > K else np.inf
+
+
+def valid_choice(key_row, chosen, K):
+    """A selection is valid if it holds every expert whose key beats the K-th key by
+    more than GAP and no expert whose key falls short of it by more than GAP."""
+    s = np.sort(key_row)[::-1]
+    kth = s[K - 1]
+    ch = set(int(e) for e in chosen)
+    if len(ch) != K:
+        return False
+    must = set(np.nonzero(key_row > kth + GAP)[0].tolist())
+    cant = set(np.nonzero(key_row < kth - GAP)[0].tolist())
+    return must <= ch and not (ch & cant)
+
+
+def tie_hook(gpu_idx_layer, K, log):
+    """Oracle route hook: on a near tie (K-th/(K+1)-th key gap <= GAP) where the
+    GPU's selection is a valid choice, continue with the GPU's selection so that
+    later computation compares like with like.  Each use is logged."""
+    def hook(t, key_row, idx_row):
+        g = np.asarray(gpu_idx_layer[t])
+        if set(g.tolist()) == set(int(v) for v in idx_row):
+            return None
+        if kth_gap(key_row, K) <= GAP and valid_choice(key_row, g, K):
+            log.append((t, sorted(g.tolist()), sorted(int(v) for v in idx_row)))
+            return g
+        return None
+    return hook
+
+
+def oracle_layer(b: Built, x, l=0, gpu_idx=None, log=None):
+    cfg = b.cfg
+    dims = helpers.oracle_dims(cfg)
+    lv = helpers.layer_view(b.model, l)
+    kc, vc = helpers.kv_view(b.kv, l)
+    hook = tie_hook(gpu_idx, cfg.top_k, log if log is not None else []) if gpu_idx is not None else None
+    return oracle.layer_forward(np.asarray(x, dtype=np.float64), lv, dims, kc, vc, b.kv.ctx[0], hook)
+
+
+def check_routing(info, gpu_idx, K, where=""):
+    """Exact match where the oracle's selection is decisive, validity elsewhere."""
+    T = gpu_idx.shape[0]
+    for t in range(T):
+        g = set(int(v) for v in gpu_idx[t])
+        o = set(int(v) for v in info["idx"][t])
+        if kth_gap(info["key"][t], K) > GAP:
+            assert g == o, "%s token %d: gpu %s oracle %s" % (where, t, sorted(g), sorted(o))
+        else:
+            assert valid_choice(info["key"][t], list(g), K), "%s token %d invalid tie choice" % (where, t)

@@ -1,0 +1,131 @@
+"""Full verify-step parity (mk_decode_step): logits, argmax, accepted count and
+per-layer routing against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from latency_moe_decode_persistent_gb300 import mk, synth
+from tests import gpu_common as gc
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+
+
+def mini_stack(**kw):
+    c = synth.Config("mini_fp8_stack", 1024, 8, 2, 128, 64, 4, 256, n_layers=3, vocab=4096,
+                     weight_dtype=synth.WDT_FP8, router_dtype=synth.WDT_BF16,
+                     kv_dtype=synth.WDT_BF16, T=6, ctx=200, seed=21)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def make_drafts(b: gc.Built, d0: int, k: int, p_accept: float, seed: int):
+    """Drafts d_1..d_k built left to right: the stack's own argmax with probability
+    p_accept, else a uniform token (prefix passes run on the GPU path)."""
+    rng = np.random.default_rng(seed)
+    toks = [d0]
+    for i in range(k):
+        _, _, am, _ = b.step(toks, trace=False)
+        a = int(am[i].item())
+        toks.append(a if rng.random() < p_accept else int(rng.integers(0, b.cfg.vocab)))
+    return toks
+
+
+def compare_step(b: gc.Built, toks):
+    logits, acc, am, trace = b.step(toks)
+    cfg = b.cfg
+    tr = trace.cpu().numpy()
+    log = []
+    dims = helpers.oracle_dims(cfg)
+    layers = [helpers.layer_view(b.model, l) for l in range(cfg.n_layers)]
+    kvs = [helpers.kv_view(b.kv, l) for l in range(cfg.n_layers)]
+    r = oracle.stack_forward(toks, helpers.embed_fn(b.model), layers,
+                             b.model.final_norm.cpu().numpy().astype(np.float64),
+                             helpers.lm_head_lin(b.model), dims, kvs, b.kv.ctx[0],
+                             route_hook_factory=lambda l: gc.tie_hook(tr[l], cfg.top_k, log))
+    for l, info in enumerate(r["layers"]):
+        gc.check_routing(info, tr[l], cfg.top_k, where="layer %d" % l)
+    lg = logits.cpu().numpy()
+    err = helpers.rel_err(lg, r["logits"])
+    ref = r["logits"]
+    rms = np.sqrt(np.mean(ref ** 2))
+    decisive = []
+    for t in range(len(toks)):
+        s = np.sort(ref[t])[::-1]
+        dec = (s[0] - s[1]) > gc.GAP * rms
+        decisive.append(dec)
+        if dec:
+            assert int(am[t]) == int(r["argmax"][t]), (t, int(am[t]), int(r["argmax"][t]))
+    if all(decisive):
+        assert acc == r["accepted"]
+    return err, acc, r, log
+
+
+def test_mini_stack_step():
+    cfg = mini_stack()
+    b = gc.Built(cfg)
+    try:
+        toks = make_drafts(b, 17, cfg.T - 1, 0.83, seed=5)
+        err, acc, r, log = compare_step(b, toks)
+        assert err < gc.TOL[synth.WDT_FP8], err
+    finally:
+        b.close()
+
+
+@pytest.mark.parametrize("T,ctx", [(1, 0), (2, 64), (8, 129)])
+def test_mini_stack_edges(T, ctx):
+    cfg = mini_stack(T=T, ctx=ctx, gamma_jitter=0.1, seed=22 + T)
+    b = gc.Built(cfg)
+    try:
+        toks = [int(v) for v in np.random.default_rng(T).integers(0, cfg.vocab, T)]
+        err, acc, r, log = compare_step(b, toks)
+        assert err < gc.TOL[synth.WDT_FP8], err
+    finally:
+        b.close()
+
+
+def test_mini_stack_all_drafts_accepted_and_deterministic():
+    cfg = mini_stack(seed=31)
+    b = gc.Built(cfg)
+    try:
+        toks = make_drafts(b, 5, cfg.T - 1, 1.0, seed=1)
+        l1, a1, am1, _ = b.step(toks, trace=False)
+        l2, a2, am2, _ = b.step(toks, trace=False)
+        assert torch.equal(l1, l2) and a1 == a2 and torch.equal(am1, am2)
+        assert a1 == cfg.T - 1
+        st = mk.mk_get_stats(b.st)
+        assert st.fused == 1 and st.launches_per_step == 1 and st.steps >= 2
+    finally:
+        b.close()
+
+
+def test_host_buffer_entry_matches_device_entry():
+    cfg = mini_stack(seed=41)
+    b = gc.Built(cfg)
+    try:
+        toks = [3, 9, 27, 81, 243, 729]
+        lg, acc, am, _ = b.step(toks, trace=False)
+        h_tok = torch.tensor(toks, dtype=torch.int32).pin_memory()
+        h_pos = torch.arange(b.kv.ctx[0], b.kv.ctx[0] + len(toks), dtype=torch.int32).pin_memory()
+        h_lg = torch.empty((len(toks), cfg.vocab), dtype=torch.float32).pin_memory()
+        h_acc = torch.zeros(1, dtype=torch.int32).pin_memory()
+        h_am = torch.zeros(len(toks), dtype=torch.int32).pin_memory()
+        mk.mk_decode_step_host(b.st, h_tok, len(toks), h_pos, b.kvargs.kv, h_lg, h_acc, h_am)
+        assert torch.equal(h_lg, lg.cpu()) and int(h_acc) == acc and torch.equal(h_am, am.cpu())
+    finally:
+        b.close()
+
+
+@pytest.mark.slow
+def test_full_43_layer_stack():
+    """The 43-layer FP8 stack, vocab 129280, T 6, ctx 2048, drafts at 0.83."""
+    cfg = synth.stack_config()
+    b = gc.Built(cfg)
+    try:
+        toks = make_drafts(b, 1000, cfg.T - 1, 0.83, seed=3)
+        err, acc, r, log = compare_step(b, toks)
+        assert err < gc.TOL[synth.WDT_FP8], err
+    finally:
+        b.close()
