@@ -193,6 +193,17 @@ mk_status mk_layer_forward(mk_state *st, int layer, const float *hidden_in, int 
  * layer against a reference. */
 mk_status mk_set_routing_trace(mk_state *st, int32_t *trace);
 
+/* Timeline of later launches: for every CTA c and grid barrier b < capacity,
+ * times[(c*capacity + b)*2] is the %globaltimer value (ns) when the CTA arrived
+ * and times[... + 1] when it left the barrier (dev uint64 [grid][capacity][2],
+ * grid = mk_stats.grid_ctas).  NULL turns it off.  Stage s of a step runs
+ * between barriers s-1 and s, so this splits the single launch into stages.
+ * events (dev uint64 [grid][1024][2], or NULL) receives (event id, time) pairs
+ * at points inside the stages: id = stage*16 + k, k = 0 inputs staged, 1 first
+ * weight tile arrived, 2 last tile reduced, 3 routing started (attention:
+ * 0 queries ready, 1 pages done, 2 group barrier passed, 3 merge done). */
+mk_status mk_set_stage_trace(mk_state *st, uint64_t *times, int capacity, uint64_t *events);
+
 /* Synchronize the last stream used and return the device status of the last
  * step (MK_OK, MK_ERR_TIMEOUT or MK_ERR_BAD_INPUT). */
 mk_status mk_get_status(mk_state *st);

@@ -32,6 +32,9 @@ struct mk_state {
     float *d_logits = nullptr;
     cudaStream_t last_stream = nullptr;
     int32_t *trace = nullptr;
+    unsigned long long *stage_trace = nullptr;
+    int stage_cap = 0;
+    unsigned long long *marks = nullptr;
     bool launched = false;
     char err[512] = {0};
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -107,7 +110,7 @@ mk_status make_mat(mk_state *st, std::vector<CUtensorMap> &maps, std::vector<lon
     d.rows = s.rows;
     d.cols = s.cols;
     d.es = dt_size(s.dtype);
-    d.n_rg = (s.rows + 127) / 128;
+    d.n_rg = (s.rows + 255) / 256;
     d.n_kc = s.cols * d.es / 128;
     d.is3d = s.E > 1;
     d.scale = s.scale;
@@ -117,7 +120,7 @@ mk_status make_mat(mk_state *st, std::vector<CUtensorMap> &maps, std::vector<lon
         if (reinterpret_cast<uintptr_t>(s.scale) % 16) return fail(st, MK_ERR_INVALID, "scale pointer not 16-byte aligned");
     }
     CUtensorMap tm;
-    mk_status r = encode_map(st, &tm, s.w, d.es, s.cols, s.rows, s.E, 128);
+    mk_status r = encode_map(st, &tm, s.w, d.es, s.cols, s.rows, s.E, 256);
     if (r != MK_OK) return r;
     map_of.push_back((long long)maps.size());
     maps.push_back(tm);
@@ -146,7 +149,7 @@ mk_status check_desc(mk_state *st, const mk_model_desc *d) {
     int kv_es = dt_size(d->kv_dtype);
     bool mma_att = d->kv_dtype == MK_DT_BF16 && d->head_dim == 128;
     if (!mma_att) {
-        if (d->head_dim * kv_es > 256) return fail(st, MK_ERR_UNSUPPORTED, "fp32 KV cache needs head_dim 64");
+        if (d->head_dim != 64) return fail(st, MK_ERR_UNSUPPORTED, "an fp32 KV cache (or head_dim 64) needs head_dim 64");
         if (G * d->max_T > 16) return fail(st, MK_ERR_UNSUPPORTED, "this KV layout supports (n_q_heads/n_kv_heads)*T <= 16");
     }
     if (d->weight_dtype < 0 || d->weight_dtype > 2) return fail(st, MK_ERR_UNSUPPORTED, "weight_dtype");
@@ -374,6 +377,9 @@ static mk_status bind_kv(mk_state *st, const mk_kv_cache *kv) {
 
 static mk_status launch(mk_state *st, Params &p, void *stream) {
     p.m = st->d_model;
+    p.stage_trace = st->stage_trace;
+    p.stage_cap = st->stage_cap;
+    p.marks = st->marks;
     p.kvmaps = st->d_kvmaps;
     p.kpool = st->d_kpool;
     p.vpool = st->d_vpool;
@@ -456,6 +462,14 @@ mk_status mk_layer_forward(mk_state *st, int layer, const float *hidden_in, int 
 mk_status mk_set_routing_trace(mk_state *st, int32_t *trace) {
     if (!st) return MK_ERR_INVALID;
     st->trace = trace;
+    return MK_OK;
+}
+
+mk_status mk_set_stage_trace(mk_state *st, uint64_t *times, int capacity, uint64_t *events) {
+    if (!st || (times && capacity < 1)) return MK_ERR_INVALID;
+    st->stage_trace = reinterpret_cast<unsigned long long *>(times);
+    st->stage_cap = times ? capacity : 0;
+    st->marks = reinterpret_cast<unsigned long long *>(events);
     return MK_OK;
 }
 

@@ -10,8 +10,10 @@
 // ---- build-time limits -----------------------------------------------------
 #define MK_NCWARPS 8                     // consumer (compute) warps per CTA
 #define MK_THREADS ((MK_NCWARPS + 1) * 32) // + one producer (TMA) warp
-#define MK_RING 8                        // shared-memory ring slots
-#define MK_SLOT 16384                    // bytes per slot: one 128-row x 128-byte TMA box
+#define MK_RING 4                        // shared-memory ring slots
+#define MK_SLOT 32768                    // bytes per slot: one 256-row x 128-byte TMA box
+#define MK_PLANES 1                      // producer lanes issuing copies side by side
+#define MK_PF 8                          // L2 prefetch distance in tiles (multiple of MK_PLANES)
 #define MK_MAXT 8                        // tokens per verify block (one N=8 MMA tile)
 #define MK_MAXKB 32                      // 128-column blocks of the widest GEMV input (4096)
 #define MK_MAXE 512                      // routed experts
@@ -19,18 +21,21 @@
 #define MK_MAXD (MK_MAXT * MK_MAXK)      // distinct experts per layer
 #define MK_MAXROWS 64                    // (q heads per kv head) x T
 #define MK_MAXSPLIT 160                  // attention splits per kv head
+#define MK_ATT_MIN_PAGES 2               // KV pages per attention split, at least
+#define MK_MARKS 1024                    // intra-stage trace events per CTA
 #define MK_FX 4294967296.0f              // fixed-point scale of the cross-CTA accumulators
 
 // Dynamic shared memory map (bytes).
 #define SM_RING 0
 #define SM_SCALE (SM_RING + MK_RING * MK_SLOT)
-#define SM_SCRATCH (SM_SCALE + MK_RING * 512)
+#define SM_SCRATCH (SM_SCALE + MK_RING * 1024)
 #define SM_SCRATCH_BYTES 65536
 #define SM_ROUTE (SM_SCRATCH + SM_SCRATCH_BYTES)
 #define SM_ROUTE_BYTES 4096
 #define SM_BAR (SM_ROUTE + SM_ROUTE_BYTES)
 #define SM_MISC (SM_BAR + 256)
-#define SM_TOTAL (SM_MISC + 256)
+#define SM_MISC_BYTES 2048
+#define SM_TOTAL (SM_MISC + SM_MISC_BYTES)
 
 // stages of one layer, in stream order
 enum { ST_QKV = 0, ST_ATT, ST_O, ST_ROUTER, ST_SHA, ST_EXPA, ST_EXPB, ST_LM };
@@ -41,7 +46,7 @@ struct DMat {
     const float *scale;        // FP8: [E][cols/128][rows]
     int dtype;                 // MK_DT_*
     int rows, cols;            // per expert
-    int n_rg;                  // 128-row groups
+    int n_rg;                  // 256-row groups
     int n_kc;                  // 128-byte column chunks
     int is3d;                  // expert stack
     int es;                    // element size (bytes)
@@ -111,6 +116,9 @@ struct Params {
     int32_t *out_idx;
     float *out_w;
     int32_t *trace;                    // [L][T][K] routing trace or null
+    unsigned long long *stage_trace;   // [G][cap][2] barrier arrive/release times or null
+    int stage_cap;
+    unsigned long long *marks;         // [G][MK_MARKS][2] (event id, time) or null
 };
 
 cudaError_t mk_launch(const Params &p, int grid, size_t smem, cudaStream_t s);

@@ -82,6 +82,18 @@ __device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int x, 
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(sa(bar))
         : "memory");
 }
+__device__ __forceinline__ void tma_prefetch2d(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_prefetch3d(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x),
+                 "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
                                          uint64_t *bar) {
     asm volatile(
@@ -136,6 +148,13 @@ __device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t v16) {
         : "r"(v16));
     return r;
 }
+// four FP8 E4M3 codes (byte 0 first) -> two f16x2 words (bytes 0,1 and 2,3)
+__device__ __forceinline__ void e4m3x4_f16(uint32_t v, uint32_t &lo, uint32_t &hi) {
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n"
+        " cvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
+        : "=r"(lo), "=r"(hi)
+        : "r"(v));
+}
 // two bf16 (low half first) -> f16x2
 __device__ __forceinline__ uint32_t bf16x2_f16x2(uint32_t v) {
     float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xffff0000u);
@@ -172,30 +191,93 @@ struct RouteSm {
     int idx[MK_MAXT][MK_MAXK];
     float w[MK_MAXT][MK_MAXK];
 };
+// CTA-uniform state in shared memory: the model block and the current/next
+// layer's descriptors are copied here so that no stage reads them from global
+// memory, and the per-thread context can be rebuilt in registers anywhere.
 struct MiscSm {
     int abort;
     int gs_ok;
     int emask[16];
     float inv_rms[3][MK_MAXT];   // attention, moe, final
     int distinct_total;
-    int valid, ctx;
-    int pad;
-    unsigned long long base;
+    int valid, ctx, nsplit;
+    int nbar;                    // grid barriers passed (thread 0)
+    int nmark;                   // trace events written (thread 0)
+    unsigned long long base;     // barrier counter at launch
+    const Params *p;
+    DModel m;
+    DLayer L[2];                 // descriptors of layers with parity 0 / 1
 };
 
 struct Ctx {
     const Params *p;
-    const DModel *m;
+    const DModel *m;             // shared-memory copy
     Ctrl *ctrl;
     unsigned char *sm;
     uint64_t *full, *empty, *route;
     RouteSm *rt;          // [2]
     MiscSm *misc;
     int cta, G, T, ctx, nsplit, tid, warp, lane;
-    unsigned long long bar_base;
-    int nbar;
     long long timeout;
+    bool prof;
 };
+
+static_assert(sizeof(MiscSm) <= SM_MISC_BYTES, "shared-memory context block too large");
+static_assert(sizeof(RouteSm) * 2 <= SM_ROUTE_BYTES, "routing block too large");
+
+__device__ __forceinline__ unsigned char *smem_base() {
+    extern __shared__ unsigned char smem_raw[];
+    // the 128-byte TMA swizzle pattern repeats every 1024 bytes: align the map to it
+    return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+}
+// the context of the calling thread, from special registers and shared memory
+__device__ __forceinline__ Ctx make_ctx() {
+    Ctx c;
+    c.sm = smem_base();
+    c.misc = reinterpret_cast<MiscSm *>(c.sm + SM_MISC);
+    c.p = c.misc->p;
+    c.m = &c.misc->m;
+    c.ctrl = c.m->ctrl;
+    c.full = reinterpret_cast<uint64_t *>(c.sm + SM_BAR);
+    c.empty = c.full + MK_RING;
+    c.route = c.empty + MK_RING;
+    c.rt = reinterpret_cast<RouteSm *>(c.sm + SM_ROUTE);
+    c.cta = blockIdx.x;
+    c.G = gridDim.x;
+    c.T = c.p->T;
+    c.ctx = c.misc->ctx;
+    c.nsplit = c.misc->nsplit;
+    c.tid = threadIdx.x;
+    c.warp = threadIdx.x >> 5;
+    c.lane = threadIdx.x & 31;
+    c.timeout = c.m->timeout_ns;
+    c.prof = c.p->marks != nullptr;
+    return c;
+}
+
+// intra-stage trace event (thread 0 of the consumers, only when tracing)
+__device__ __forceinline__ void mark(const Ctx &c, int id) {
+    const Params &p = *c.p;
+    if (p.marks && c.tid == 0) {
+        const int k = c.misc->nmark;
+        if (k < MK_MARKS - 80) {
+            unsigned long long *e = p.marks + ((long long)c.cta * MK_MARKS + k) * 2;
+            e[0] = (unsigned long long)id;
+            e[1] = gtimer();
+        }
+        c.misc->nmark = k + 1;
+    }
+}
+
+// trace value written at a fixed event slot (cycle counts of a loop)
+__device__ __forceinline__ void mark_val(const Ctx &c, int slot, int id, unsigned long long v) {
+    const Params &p = *c.p;
+    if (p.marks && slot < MK_MARKS) {
+        unsigned long long *e = p.marks + ((long long)c.cta * MK_MARKS + slot) * 2;
+        e[0] = (unsigned long long)id;
+        e[1] += v;
+    }
+}
 
 __device__ __forceinline__ bool aborted(const Ctx &c) {
     return *(volatile int *)&c.misc->abort != 0 || *(volatile int *)&c.ctrl->abort != 0;
@@ -264,26 +346,32 @@ __device__ bool spin_ge_s32(int *a, int target, const Ctx &c, int where) {
 }
 
 // grid-wide barrier among the consumer warps of all CTAs; split into arrive/wait
-__device__ void grid_arrive(Ctx &c) {
+__device__ void grid_arrive(const Ctx &c) {
     bar_consumers();
-    c.nbar++;
     if (c.tid == 0) {
+        const int nbar = ++c.misc->nbar;
+        const Params &p = *c.p;
+        if (p.stage_trace && nbar <= p.stage_cap)
+            p.stage_trace[((long long)c.cta * p.stage_cap + nbar - 1) * 2] = gtimer();
         __threadfence();
         atomicAdd(&c.ctrl->bar_count, 1ull);
     }
 }
-__device__ bool grid_wait(Ctx &c, int where) {
+__device__ bool grid_wait(const Ctx &c, int where) {
     if (c.tid == 0) {
+        const int nbar = c.misc->nbar;
         bool ok = !aborted(c);
-        if (ok) ok = spin_ge_u64(&c.ctrl->bar_count, c.bar_base + (unsigned long long)c.nbar * c.G, c,
-                                 where);
+        if (ok) ok = spin_ge_u64(&c.ctrl->bar_count, c.misc->base + (unsigned long long)nbar * c.G, c, where);
         __threadfence();
         c.misc->gs_ok = ok && !aborted(c);
+        const Params &p = *c.p;
+        if (p.stage_trace && nbar <= p.stage_cap)
+            p.stage_trace[((long long)c.cta * p.stage_cap + nbar - 1) * 2 + 1] = gtimer();
     }
     bar_consumers();
     return c.misc->gs_ok != 0;
 }
-__device__ bool grid_sync(Ctx &c, int where) {
+__device__ bool grid_sync(const Ctx &c, int where) {
     grid_arrive(c);
     return grid_wait(c, where);
 }
@@ -379,83 +467,247 @@ __device__ AttUnit att_unit(const Ctx &c) {
     return u;
 }
 
-// ------------------------------------------------------------------ producer
-__device__ bool prod_slot(Ctx &c, uint32_t &pi, uint32_t bytes, uint32_t &slot) {
-    slot = pi % MK_RING;
-    if (!mbar_wait(&c.empty[slot], ((pi / MK_RING) & 1) ^ 1, c, 100)) return false;
-    mbar_expect_tx(&c.full[slot], bytes);
-    return true;
+// register copy of the matrix-descriptor fields the tile loops use
+struct MatR {
+    const CUtensorMap *tmap;
+    const float *scale;
+    long long sest;
+    int rows, cols, xstep, dtype, is3d;
+};
+__device__ __forceinline__ MatR mat_regs(const DMat &d) {
+    MatR r;
+    r.tmap = d.tmap;
+    r.scale = d.scale;
+    r.sest = d.scale_estride;
+    r.rows = d.rows;
+    r.cols = d.cols;
+    r.xstep = d.es ? 128 / d.es : 128;
+    r.dtype = d.dtype;
+    r.is3d = d.is3d;
+    return r;
 }
 
-__device__ bool prod_gemv(Ctx &c, int st, const DLayer &L, const RouteSm *rt, uint32_t &pi) {
-    const DModel &m = *c.m;
-    int b, e;
-    split_range(stage_total(m, st, L, rt), c.G, c.cta, b, e);
-    for (int idx = b; idx < e; ++idx) {
-        Item it = stage_item(m, st, L, rt, idx);
-        const DMat &d = *it.m;
-        uint32_t sbytes = 0;
-        if (d.dtype == MK_DT_FP8E4M3_B128) sbytes = min(128, d.rows - it.rg * 128) * 4;
-        uint32_t slot;
-        if (!prod_slot(c, pi, MK_SLOT + sbytes, slot)) return false;
-        void *dst = c.sm + SM_RING + slot * MK_SLOT;
-        int x = it.kc * (128 / d.es);
-        if (d.is3d) tma3d(dst, d.tmap, x, it.rg * 128, it.e, &c.full[slot]);
-        else tma2d(dst, d.tmap, x, it.rg * 128, &c.full[slot]);
-        if (sbytes) {
-            const float *src = d.scale + (long long)it.e * d.scale_estride +
-                               (long long)it.kc * d.rows + it.rg * 128;
-            bulk_g2s(c.sm + SM_SCALE + slot * 512, src, sbytes, &c.full[slot]);
-        }
-        ++pi;
+// Walks the tiles of one stage that belong to this CTA, in (expert slot,
+// matrix, 128-row group, 128-byte column chunk) order.  Descriptors are read
+// once per stage; the position advances with counters, no divisions.
+struct StageIter {
+    MatR m0, m1;          // matrix 0 / 1 (gate/up pairs; routed/shared down)
+    int n_rg, n_kc, nmat, nex, nd;
+    int ex, mat, rg, kc, n;
+    int st;
+    const int *dlist;
+    __device__ __forceinline__ const MatR &cur() const {
+        return (st == ST_EXPB ? ex >= nd : mat != 0) ? m1 : m0;
     }
+    __device__ __forceinline__ int expert() const {
+        return (st == ST_EXPA || (st == ST_EXPB && ex < nd)) ? dlist[ex] : 0;
+    }
+    __device__ __forceinline__ void advance() {
+        if (++kc == n_kc) {
+            kc = 0;
+            if (++rg == n_rg) {
+                rg = 0;
+                if (++mat == nmat) {
+                    mat = 0;
+                    ++ex;
+                }
+            }
+        }
+    }
+};
+
+__device__ void stage_iter(StageIter &it, const Ctx &c, int st, const DLayer &L, const RouteSm *rt) {
+    const DModel &m = *c.m;
+    it.st = st;
+    it.nmat = 1;
+    it.nex = 1;
+    it.nd = 0;
+    it.dlist = rt->dlist;
+    switch (st) {
+        case ST_QKV: it.m0 = mat_regs(L.qkv); break;
+        case ST_O: it.m0 = mat_regs(L.o); break;
+        case ST_ROUTER: it.m0 = mat_regs(L.router); break;
+        case ST_LM: it.m0 = mat_regs(m.lm); break;
+        case ST_SHA:
+            it.m0 = mat_regs(L.s1);
+            it.m1 = mat_regs(L.s3);
+            it.nmat = 2;
+            it.nex = m.nshared;
+            break;
+        case ST_EXPA:
+            it.m0 = mat_regs(L.w1);
+            it.m1 = mat_regs(L.w3);
+            it.nmat = 2;
+            it.nex = rt->nd;
+            it.nd = rt->nd;
+            break;
+        default:  // ST_EXPB
+            it.m0 = mat_regs(L.w2);
+            it.m1 = mat_regs(L.s2);
+            it.nd = rt->nd;
+            it.nex = rt->nd + m.nshared;
+            break;
+    }
+    const DMat &d0 = st == ST_QKV ? L.qkv : st == ST_O ? L.o : st == ST_ROUTER ? L.router :
+                     st == ST_LM ? m.lm : st == ST_SHA ? L.s1 : st == ST_EXPA ? L.w1 : L.w2;
+    it.n_rg = d0.n_rg;
+    it.n_kc = d0.n_kc;
+    const int per_mat = it.n_rg * it.n_kc, per_ex = it.nmat * per_mat;
+    int b, e;
+    split_range(it.nex * per_ex, c.G, c.cta, b, e);
+    it.n = e - b;
+    it.ex = b / per_ex;
+    int r = b - it.ex * per_ex;
+    it.mat = r / per_mat;
+    r -= it.mat * per_mat;
+    it.rg = r / it.n_kc;
+    it.kc = r - it.rg * it.n_kc;
+}
+
+// ------------------------------------------------------------------ producer
+// MK_PLANES lanes of the producer warp issue copies side by side: lane j takes
+// the stage's tiles j, j + MK_PLANES, ...  With MK_PLANES == MK_RING every lane
+// owns one ring slot, so four tiles are requested concurrently while each lane
+// keeps its own wait -> arm -> copy chain.
+
+// producer-side state of one issuing lane (registers of the producer)
+struct Prod {
+    uint32_t pi;                  // ring positions handed out so far
+    int last;                     // last position this lane armed (-1: none)
+    unsigned long long wait, tma, bulk;
+};
+
+// wait for ring position pos to be free and arm its full barrier for `bytes`
+__device__ __forceinline__ bool prod_take(const Ctx &c, Prod &ps, uint32_t pos, uint32_t bytes) {
+    const uint32_t slot = pos % MK_RING;
+    unsigned long long cy1 = c.prof ? clock64() : 0;
+    if (!mbar_wait(&c.empty[slot], ((pos / MK_RING) & 1) ^ 1, c, 100)) return false;
+    if (c.prof) ps.wait += clock64() - cy1;
+    mbar_expect_tx(&c.full[slot], bytes);
+    ps.last = (int)pos;
     return true;
 }
 
-__device__ bool prod_att(Ctx &c, int l, uint32_t &pi) {
+// L2 prefetch of the tile at the iterator's position (weights and FP8 scales)
+__device__ __forceinline__ void prefetch_tile(const StageIter &it) {
+    const MatR &d = it.cur();
+    const int e = it.expert();
+    const int x = it.kc * d.xstep, y = it.rg * 256;
+    if (d.is3d) tma_prefetch3d(d.tmap, x, y, e);
+    else tma_prefetch2d(d.tmap, x, y);
+    if (d.dtype == MK_DT_FP8E4M3_B128)
+        bulk_prefetch(d.scale + (long long)e * d.sest + (long long)it.kc * d.rows + y, min(256, d.rows - y) * 4);
+}
+
+__device__ __forceinline__ bool prod_gemv_impl(const Ctx &c, Prod &ps, int st, const DLayer &L,
+                                               const RouteSm *rt) {
+    StageIter it;
+    stage_iter(it, c, st, L, rt);
+    const int n = it.n;
+    for (int j = 0; j < c.lane && j < n; ++j) it.advance();
+    unsigned char *const ring = c.sm + SM_RING, *const sbase = c.sm + SM_SCALE;
+    uint64_t *const full = c.full;
+    bool ok = true;
+    for (int t = c.lane; t < n; t += MK_PLANES) {
+        const MatR &d = it.cur();
+        const int e = it.expert();
+        uint32_t sbytes = 0;
+        if (d.dtype == MK_DT_FP8E4M3_B128) sbytes = min(256, d.rows - it.rg * 256) * 4;
+        const uint32_t pos = ps.pi + t, slot = pos % MK_RING;
+        if (!prod_take(c, ps, pos, MK_SLOT + sbytes)) {
+            ok = false;
+            break;
+        }
+        void *dst = ring + slot * MK_SLOT;
+        const int x = it.kc * d.xstep, y = it.rg * 256;
+        unsigned long long t0 = c.prof ? clock64() : 0;
+        if (d.is3d) tma3d(dst, d.tmap, x, y, e, &full[slot]);
+        else tma2d(dst, d.tmap, x, y, &full[slot]);
+        unsigned long long t1 = c.prof ? clock64() : 0;
+        if (sbytes) {
+            const float *src = d.scale + (long long)e * d.sest + (long long)it.kc * d.rows + y;
+            bulk_g2s(sbase + slot * 1024, src, sbytes, &full[slot]);
+        }
+        if (c.prof) {
+            unsigned long long t2 = clock64();
+            ps.tma += t1 - t0;
+            ps.bulk += t2 - t1;
+        }
+#pragma unroll
+        for (int j = 0; j < MK_PLANES; ++j) it.advance();
+    }
+    ps.pi += n;
+    // every lane has issued its tiles of this stage before any lane starts the
+    // next one, so no slot's empty barrier is ever waited on two phases ahead
+    return __all_sync((1u << MK_PLANES) - 1, ok);
+}
+
+__device__ __forceinline__ bool prod_gemv(const Ctx &c, Prod &ps, int st, const DLayer &L, const RouteSm *rt) {
+    const bool prof = c.prof && c.lane == 0;
+    unsigned long long cy0 = prof ? clock64() : 0, w0 = ps.wait, a0 = ps.tma, b0 = ps.bulk;
+    bool ok = prod_gemv_impl(c, ps, st, L, rt);
+    if (prof) {
+        mark_val(c, MK_MARKS - 32 + st * 2 + 0, 950 + st * 2 + 0, ps.wait - w0);
+        mark_val(c, MK_MARKS - 32 + st * 2 + 1, 950 + st * 2 + 1, clock64() - cy0);
+        mark_val(c, MK_MARKS - 16 + st * 2 + 0, 980 + st * 2 + 0, ps.tma - a0);
+        mark_val(c, MK_MARKS - 16 + st * 2 + 1, 980 + st * 2 + 1, ps.bulk - b0);
+    }
+    return ok;
+}
+
+// this CTA's KV pages of one layer: K in the first half of a slot, V in the second
+__device__ __forceinline__ bool prod_att(const Ctx &c, Prod &ps, int l) {
     const DModel &m = *c.m;
     AttUnit u = att_unit(c);
-    if (!u.active) return true;
-    int nbox = (m.d * m.kv_es) / 128;
+    if (!u.active) return true;  // uniform across the producer lanes
+    const int nbox = (m.d * m.kv_es) / 128;
     const CUtensorMap *km = c.p->kvmaps + 2 * l, *vm = km + 1;
-    for (int j = u.p0; j < u.pc1; ++j) {
-        int phys = __ldg(c.p->page_table + j);
-        int y = (phys * m.Hkv + u.g) * m.P;
-        for (int kv = 0; kv < 2; ++kv) {
-            uint32_t slot;
-            if (!prod_slot(c, pi, nbox * m.P * 128, slot)) return false;
-            unsigned char *dst = c.sm + SM_RING + slot * MK_SLOT;
-            for (int bx = 0; bx < nbox; ++bx)
-                tma2d(dst + bx * m.P * 128, kv ? vm : km, bx * (128 / m.kv_es), y, &c.full[slot]);
-            ++pi;
+    bool ok = true;
+    for (int j = u.p0 + c.lane; j < u.pc1; j += MK_PLANES) {
+        const int phys = __ldg(c.p->page_table + j);
+        const int y = (phys * m.Hkv + u.g) * m.P;
+        const uint32_t pos = ps.pi + (j - u.p0);
+        if (!prod_take(c, ps, pos, 2 * nbox * m.P * 128)) {
+            ok = false;
+            break;
+        }
+        unsigned char *dst = c.sm + SM_RING + (pos % MK_RING) * MK_SLOT;
+        uint64_t *bar = &c.full[pos % MK_RING];
+        for (int bx = 0; bx < nbox; ++bx) {
+            tma2d(dst + bx * m.P * 128, km, bx * (128 / m.kv_es), y, bar);
+            tma2d(dst + MK_SLOT / 2 + bx * m.P * 128, vm, bx * (128 / m.kv_es), y, bar);
         }
     }
-    return true;
+    ps.pi += u.pc1 - u.p0;
+    return __all_sync((1u << MK_PLANES) - 1, ok);
 }
 
-__device__ void producer(Ctx &c) {
+// lanes 0..MK_PLANES-1 of the producer warp
+__device__ __noinline__ void producer() {
+    const Ctx c = make_ctx();
     const DModel &m = *c.m;
     const Params &p = *c.p;
-    uint32_t pi = 0;
+    Prod ps;
+    ps.pi = 0;
+    ps.last = -1;
+    ps.wait = ps.tma = ps.bulk = 0;
     int nl = p.mode ? 1 : m.L;
     bool ok = true;
     for (int li = 0; li < nl && ok; ++li) {
         int l = p.mode ? p.layer : li;
-        const DLayer &L = m.layers[l];
+        const DLayer &L = c.misc->L[li & 1];
         const RouteSm *rt = &c.rt[li & 1];
-        ok = prod_gemv(c, ST_QKV, L, rt, pi) && prod_att(c, l, pi) &&
-             prod_gemv(c, ST_O, L, rt, pi) && prod_gemv(c, ST_ROUTER, L, rt, pi) &&
-             prod_gemv(c, ST_SHA, L, rt, pi);
+        ok = prod_gemv(c, ps, ST_QKV, L, rt) && prod_att(c, ps, l) && prod_gemv(c, ps, ST_O, L, rt) &&
+             prod_gemv(c, ps, ST_ROUTER, L, rt) && prod_gemv(c, ps, ST_SHA, L, rt);
         if (!ok) break;
-        if (!mbar_wait(c.route, li & 1, c, 101)) { ok = false; break; }
-        ok = prod_gemv(c, ST_EXPA, L, rt, pi) && prod_gemv(c, ST_EXPB, L, rt, pi);
+        ok = __all_sync((1u << MK_PLANES) - 1, mbar_wait(c.route, li & 1, c, 101));
+        if (!ok) break;
+        ok = prod_gemv(c, ps, ST_EXPA, L, rt) && prod_gemv(c, ps, ST_EXPB, L, rt);
     }
-    if (ok && p.mode == 0) ok = prod_gemv(c, ST_LM, m.layers[0], &c.rt[0], pi);
-    if (!ok) {
-        // copies still in flight must land before the CTA may exit
-        for (uint32_t i = (pi > MK_RING ? pi - MK_RING : 0); i < pi; ++i)
-            mbar_wait_drain(&c.full[i % MK_RING], (i / MK_RING) & 1, c);
-    }
+    if (ok && p.mode == 0) ok = prod_gemv(c, ps, ST_LM, c.misc->L[0], &c.rt[0]);
+    // after a failure, the last copy this lane issued must land before the CTA exits
+    // (earlier copies into the same slot completed before it was re-armed)
+    if (!ok && ps.last >= 0) mbar_wait_drain(&c.full[ps.last % MK_RING], (ps.last / MK_RING) & 1, c);
 }
 
 // ------------------------------------------------------------------ activations
@@ -476,32 +728,86 @@ struct ActSrc {
     int stride;
     const float *gamma;
 };
-__device__ __forceinline__ float act_val(const ActSrc &a, int t, int col) {
-    float v = a.fx ? from_fx(__ldcg(a.fx + (long long)t * a.stride + col))
-                   : __ldcg(a.f32 + (long long)t * a.stride + col);
-    return a.gamma ? v * __ldg(a.gamma + col) : v;
+// four consecutive activation values from column col (col % 4 == 0)
+__device__ __forceinline__ float4 act4(const ActSrc &a, int t, int col) {
+    float4 v;
+    if (a.fx) {
+        const longlong2 *p = reinterpret_cast<const longlong2 *>(a.fx + (long long)t * a.stride + col);
+        longlong2 x = __ldcg(p), y = __ldcg(p + 1);
+        v = make_float4(from_fx(x.x), from_fx(x.y), from_fx(y.x), from_fx(y.y));
+    } else {
+        v = __ldcg(reinterpret_cast<const float4 *>(a.f32 + (long long)t * a.stride + col));
+    }
+    if (a.gamma) {
+        float4 g = __ldg(reinterpret_cast<const float4 *>(a.gamma + col));
+        v.x *= g.x;
+        v.y *= g.y;
+        v.z *= g.z;
+        v.w *= g.w;
+    }
+    return v;
 }
 
-// build f16 fragments for the 128-column blocks in `mask` (consumer threads)
-__device__ void build_frags(const Ctx &c, const ActSrc &a, uint32_t mask, int kb0 = 0) {
-    unsigned char *fr = c.sm + SM_SCRATCH;
+// build f16 fragments for the 128-column blocks in `mask` (consumer threads);
+// loads of eight blocks are issued before any is converted
+__device__ __noinline__ void build_frags(const ActSrc a, uint32_t mask) {
+    const Ctx c = make_ctx();
     const int s = c.tid >> 5, l = c.lane, n = l >> 2, q = l & 3;
-    for (int kb = 0; kb < MK_MAXKB; ++kb) {
-        if (!((mask >> kb) & 1)) continue;
-        float v[4];
+    const int col0 = frag_col(s, q, 0);
+    unsigned char *fr = c.sm + SM_SCRATCH + ((s >> 1) * 32 + l) * 16 + (s & 1) * 8;
+    const bool live = n < c.T;
+    const long long *fx = a.fx ? a.fx + (long long)n * a.stride + col0 : nullptr;
+    const float *f32 = a.f32 ? a.f32 + (long long)n * a.stride + col0 : nullptr;
+    for (int base = 0; base < MK_MAXKB; base += 4) {
+        const uint32_t mb = (mask >> base) & 0xfu;
+        if (!mb) continue;
+        longlong2 r0[4], r1[4];
+        float4 rf[4], g[4];
+        // phase 1: every load of the batch in flight
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            v[j] = (n < c.T) ? act_val(a, n, (kb + kb0) * 128 + frag_col(s, q, j)) : 0.f;
-        uint2 w = make_uint2(pack_f16(v[0], v[1]), pack_f16(v[2], v[3]));
-        *reinterpret_cast<uint2 *>(fr + kb * 2048 + ((s >> 1) * 32 + l) * 16 + (s & 1) * 8) = w;
+        for (int i = 0; i < 4; ++i) {
+            const int col = (base + i) * 128;
+            r0[i] = r1[i] = make_longlong2(0, 0);
+            rf[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            g[i] = make_float4(1.f, 1.f, 1.f, 1.f);
+            if (((mb >> i) & 1) && live) {
+                if (fx) {
+                    r0[i] = __ldcg(reinterpret_cast<const longlong2 *>(fx + col));
+                    r1[i] = __ldcg(reinterpret_cast<const longlong2 *>(fx + col) + 1);
+                } else {
+                    rf[i] = __ldcg(reinterpret_cast<const float4 *>(f32 + col));
+                }
+                if (a.gamma) g[i] = __ldg(reinterpret_cast<const float4 *>(a.gamma + col0 + col));
+            }
+        }
+        // phase 2: convert and store
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (!((mb >> i) & 1)) continue;
+            float4 v = fx ? make_float4(from_fx(r0[i].x), from_fx(r0[i].y), from_fx(r1[i].x), from_fx(r1[i].y)) : rf[i];
+            *reinterpret_cast<uint2 *>(fr + (base + i) * 2048) =
+                make_uint2(pack_f16(v.x * g[i].x, v.y * g[i].y), pack_f16(v.z * g[i].z, v.w * g[i].w));
+        }
     }
 }
 // f32 activations [MK_MAXT][K] for the FFMA path
-__device__ void build_act32(const Ctx &c, const ActSrc &a, int K) {
-    float *dst = reinterpret_cast<float *>(c.sm + SM_SCRATCH);
-    for (int i = c.tid; i < MK_MAXT * K; i += MK_NCWARPS * 32) {
-        int t = i / K, col = i - t * K;
-        dst[i] = t < c.T ? act_val(a, t, col) : 0.f;
+__device__ __noinline__ void build_act32(const ActSrc a, int K) {
+    const Ctx c = make_ctx();
+    float4 *dst = reinterpret_cast<float4 *>(c.sm + SM_SCRATCH);
+    const int n4 = MK_MAXT * K / 4;
+    for (int i0 = c.tid; i0 < n4; i0 += 4 * MK_NCWARPS * 32) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            int i = i0 + u * MK_NCWARPS * 32;
+            int t = (4 * i) / K, col = 4 * i - t * K;
+            v[u] = (i < n4 && t < c.T) ? act4(a, t, col) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            int i = i0 + u * MK_NCWARPS * 32;
+            if (i < n4) dst[i] = v[u];
+        }
     }
 }
 
@@ -517,161 +823,155 @@ __device__ uint32_t needed_kb(int b, int e, const DMat &d) {
 }
 
 // ------------------------------------------------------------------ GEMV tiles
+// where the partial sums of one item go: token t's row r adds w * value into
+// base[off(t) + r], with off(t) < 0 meaning token t does not take part
 struct Tgt {
     long long *base;
-    int toff[MK_MAXT];
-    float tw[MK_MAXT];
-    int row_limit;
+    int st, tstride, ex, K2I, row_limit;
+    const RouteSm *rt;
 };
-
-__device__ void make_tgt(const Ctx &c, int st, const Item &it, const RouteSm *rt, Tgt &g) {
+__device__ __forceinline__ Tgt make_tgt(const Ctx &c, int st, int ex, int mat, int rows, const RouteSm *rt) {
     const DModel &m = *c.m;
-    for (int t = 0; t < MK_MAXT; ++t) {
-        g.toff[t] = -1;
-        g.tw[t] = 1.f;
-    }
-    g.row_limit = it.m->rows;
+    Tgt g;
+    g.st = st;
+    g.ex = ex;
+    g.rt = rt;
+    g.row_limit = rows;
+    g.K2I = m.K * 2 * m.I;
     switch (st) {
-        case ST_QKV:
-            g.base = m.qkv_acc;
-            for (int t = 0; t < c.T; ++t) g.toff[t] = t * m.nqkv;
-            break;
-        case ST_O:
-            g.base = m.res;
-            for (int t = 0; t < c.T; ++t) g.toff[t] = t * m.H;
-            break;
-        case ST_ROUTER:
-            g.base = m.rlog;
-            for (int t = 0; t < c.T; ++t) g.toff[t] = t * m.E;
-            break;
-        case ST_SHA:
-            g.base = m.sh_acc + it.mat * m.I;
-            for (int t = 0; t < c.T; ++t) g.toff[t] = t * 2 * m.I;
-            break;
-        case ST_EXPA:
-            g.base = m.ea_acc + it.mat * m.I;
-            for (int t = 0; t < c.T; ++t) {
-                int j = rt->dslot[it.ex][t];
-                if (j >= 0) g.toff[t] = (t * m.K + j) * 2 * m.I;
-            }
-            break;
-        case ST_EXPB:
-            g.base = m.res;
-            for (int t = 0; t < c.T; ++t) {
-                if (it.ex < rt->nd) {
-                    int j = rt->dslot[it.ex][t];
-                    if (j >= 0) {
-                        g.toff[t] = t * m.H;
-                        g.tw[t] = rt->w[t][j];
-                    }
-                } else {
-                    g.toff[t] = t * m.H;
-                }
-            }
-            break;
-        case ST_LM:
-            g.base = m.logit_acc;
-            for (int t = 0; t < c.T; ++t) g.toff[t] = t * m.V;
-            break;
+        case ST_QKV: g.base = m.qkv_acc; g.tstride = m.nqkv; break;
+        case ST_O: g.base = m.res; g.tstride = m.H; break;
+        case ST_ROUTER: g.base = m.rlog; g.tstride = m.E; break;
+        case ST_SHA: g.base = m.sh_acc + mat * m.I; g.tstride = 2 * m.I; break;
+        case ST_EXPA: g.base = m.ea_acc + mat * m.I; g.tstride = 2 * m.I; break;
+        case ST_EXPB: g.base = m.res; g.tstride = m.H; break;
+        default: g.base = m.logit_acc; g.tstride = m.V; break;
     }
+    return g;
+}
+// offset of token t (< 0: not routed) and its weight
+__device__ __forceinline__ int tgt_off(const Tgt &g, int t, int T, float &w) {
+    w = 1.f;
+    if (t >= T) return -1;
+    if (g.st == ST_EXPA) {
+        int j = g.rt->dslot[g.ex][t];
+        return j < 0 ? -1 : t * g.K2I + j * g.tstride;
+    }
+    if (g.st == ST_EXPB && g.ex < g.rt->nd) {
+        int j = g.rt->dslot[g.ex][t];
+        if (j < 0) return -1;
+        w = g.rt->w[t][j];
+    }
+    return t * g.tstride;
 }
 
-// MMA layout: lane holds rows (r, r+8) x tokens (2q, 2q+1) of the warp's 16 rows
-__device__ void flush_mma(const Ctx &c, const Tgt &g, int row0, const float *acc) {
+// MMA layout: for m-tile mt (0, 1) of the warp's 32 rows, lane holds rows
+// (16mt + r, 16mt + r + 8) x tokens (2q, 2q+1) in acc[4mt .. 4mt+3]
+__device__ __forceinline__ void flush_mma(const Ctx &c, const Tgt &g, int row0, const float *acc) {
     const int r = c.lane >> 2, q = c.lane & 3;
+    float w0, w1;
+    const int o0 = tgt_off(g, 2 * q, c.T, w0), o1 = tgt_off(g, 2 * q + 1, c.T, w1);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int t = 2 * q + (i & 1);
-        int row = row0 + r + (i >> 1) * 8;
-        if (t < MK_MAXT && g.toff[t] >= 0 && row < g.row_limit)
-            red_add(g.base + g.toff[t] + row, to_fx(acc[i] * g.tw[t]));
+    for (int i = 0; i < 8; ++i) {
+        const int o = (i & 1) ? o1 : o0;
+        const float w = (i & 1) ? w1 : w0;
+        const int row = row0 + (i >> 2) * 16 + r + ((i >> 1) & 1) * 8;
+        if (o >= 0 && row < g.row_limit) red_add(g.base + o + row, to_fx(acc[i] * w));
     }
 }
-// FFMA layout: lanes 0..15 hold one row each, all tokens
-__device__ void flush_f32(const Ctx &c, const Tgt &g, int row0, float *acc) {
-    // lanes l and l+16 hold the two column halves of the same row
-#pragma unroll
-    for (int t = 0; t < MK_MAXT; ++t) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 16);
-    if (c.lane >= 16) return;
+// FFMA layout: lane l holds row l of the warp's 32 rows, all tokens
+__device__ __forceinline__ void flush_f32(const Ctx &c, const Tgt &g, int row0, const float *acc) {
     int row = row0 + c.lane;
     if (row >= g.row_limit) return;
 #pragma unroll
-    for (int t = 0; t < MK_MAXT; ++t)
-        if (g.toff[t] >= 0) red_add(g.base + g.toff[t] + row, to_fx(acc[t] * g.tw[t]));
+    for (int t = 0; t < MK_MAXT; ++t) {
+        float w;
+        const int o = tgt_off(g, t, c.T, w);
+        if (o >= 0) red_add(g.base + o + row, to_fx(acc[t] * w));
+    }
 }
 
-// one 128-row x 128-byte tile of FP8 or bf16 weights against the f16 fragments
-__device__ __forceinline__ void tile_mma(const Ctx &c, const DMat &d, int slot, int kc,
-                                         float *acc) {
+// one 256-row x 128-byte tile of FP8 or bf16 weights against the f16 fragments;
+// warp w reduces rows 32w..32w+31 as two 16-row MMA tiles
+__device__ __forceinline__ void tile_mma(const Ctx &c, int dtype, int slot, int kc, float *acc) {
     const int r = c.lane >> 2, q = c.lane & 3;
     const uint32_t tile = sa(c.sm + SM_RING + slot * MK_SLOT);
-    const int row0 = c.warp * 16 + r, row8 = row0 + 8;
+    const int rw = c.warp * 32 + r;  // rows rw, rw+8 (tile 0), rw+16, rw+24 (tile 1); all = r mod 8
     const uint32_t frag = sa(c.sm + SM_SCRATCH);
-    if (d.dtype == MK_DT_FP8E4M3_B128) {
-        const int ca = 2 * q + (q >> 1), cb = 2 * q + 1 - (q >> 1);
-        uint4 a0 = lds128(tile + row0 * 128 + ((ca ^ r) << 4));
-        uint4 a1 = lds128(tile + row0 * 128 + ((cb ^ r) << 4));
-        uint4 b0 = lds128(tile + row8 * 128 + ((ca ^ r) << 4));
-        uint4 b1 = lds128(tile + row8 * 128 + ((cb ^ r) << 4));
+    if (dtype == MK_DT_FP8E4M3_B128) {
+        const int ca = ((2 * q + (q >> 1)) ^ r) << 4, cb = ((2 * q + 1 - (q >> 1)) ^ r) << 4;
+        uint4 a[4][2];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            a[j][0] = lds128(tile + (rw + 8 * j) * 128 + ca);
+            a[j][1] = lds128(tile + (rw + 8 * j) * 128 + cb);
+        }
         const uint32_t fb = frag + kc * 2048 + c.lane * 16;
         uint4 f0 = lds128(fb), f1 = lds128(fb + 512), f2 = lds128(fb + 1024), f3 = lds128(fb + 1536);
-        float k4[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t w0[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const uint32_t w8[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
         const uint32_t fx[8] = {f0.x, f0.z, f1.x, f1.z, f2.x, f2.z, f3.x, f3.z};
         const uint32_t fy[8] = {f0.y, f0.w, f1.y, f1.w, f2.y, f2.w, f3.y, f3.w};
+        float k[4][4];  // [tile*2 + chain][4]
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            mma_f16(k4, e4m3x2_f16x2(w0[s] & 0xffff), e4m3x2_f16x2(w8[s] & 0xffff),
-                    e4m3x2_f16x2(w0[s] >> 16), e4m3x2_f16x2(w8[s] >> 16), fx[s], fy[s]);
+        for (int i = 0; i < 4; ++i) k[i][0] = k[i][1] = k[i][2] = k[i][3] = 0.f;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const uint4 &u0 = a[2 * mt][s2 >> 2], &u8 = a[2 * mt + 1][s2 >> 2];
+                const uint32_t w0 = (s2 & 3) == 0 ? u0.x : (s2 & 3) == 1 ? u0.y : (s2 & 3) == 2 ? u0.z : u0.w;
+                const uint32_t w8 = (s2 & 3) == 0 ? u8.x : (s2 & 3) == 1 ? u8.y : (s2 & 3) == 2 ? u8.z : u8.w;
+                uint32_t lo0, hi0, lo8, hi8;
+                e4m3x4_f16(w0, lo0, hi0);
+                e4m3x4_f16(w8, lo8, hi8);
+                mma_f16(k[2 * mt + (s2 & 1)], lo0, lo8, hi0, hi8, fx[s2], fy[s2]);
+            }
         }
-        const float *sc = reinterpret_cast<const float *>(c.sm + SM_SCALE + slot * 512);
-        float s0 = sc[row0], s8 = sc[row8];
-        acc[0] += k4[0] * s0;
-        acc[1] += k4[1] * s0;
-        acc[2] += k4[2] * s8;
-        acc[3] += k4[3] * s8;
+        const float *sc = reinterpret_cast<const float *>(c.sm + SM_SCALE + slot * 1024);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            const float s0 = sc[rw + 16 * mt], s8 = sc[rw + 16 * mt + 8];
+            acc[4 * mt + 0] += (k[2 * mt][0] + k[2 * mt + 1][0]) * s0;
+            acc[4 * mt + 1] += (k[2 * mt][1] + k[2 * mt + 1][1]) * s0;
+            acc[4 * mt + 2] += (k[2 * mt][2] + k[2 * mt + 1][2]) * s8;
+            acc[4 * mt + 3] += (k[2 * mt][3] + k[2 * mt + 1][3]) * s8;
+        }
     } else {  // bf16: the tile is half of a 128-column block
         const int h = kc & 1, kb = kc >> 1;
         const bool act = (q >> 1) == h;
         const int qq = q & 1;
-        uint4 ra[4], rb[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            int ch = 4 * qq + ((i + 2 * h) & 3);
-            if (act) {
-                ra[i] = lds128(tile + row0 * 128 + ((ch ^ r) << 4));
-                rb[i] = lds128(tile + row8 * 128 + ((ch ^ r) << 4));
-            } else {
-                ra[i] = make_uint4(0, 0, 0, 0);
-                rb[i] = make_uint4(0, 0, 0, 0);
-            }
-        }
         const uint32_t fb = frag + kb * 2048 + c.lane * 16;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
+            const int ch = ((4 * qq + ((i + 2 * h) & 3)) ^ r) << 4;
+            uint4 ra[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                ra[j] = act ? lds128(tile + (rw + 8 * j) * 128 + ch) : make_uint4(0, 0, 0, 0);
             uint4 f = lds128(fb + i * 512);
-            mma_f16(acc, bf16x2_f16x2(ra[i].x), bf16x2_f16x2(rb[i].x), bf16x2_f16x2(ra[i].y),
-                    bf16x2_f16x2(rb[i].y), f.x, f.y);
-            mma_f16(acc, bf16x2_f16x2(ra[i].z), bf16x2_f16x2(rb[i].z), bf16x2_f16x2(ra[i].w),
-                    bf16x2_f16x2(rb[i].w), f.z, f.w);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const uint4 &x0 = ra[2 * mt], &x8 = ra[2 * mt + 1];
+                mma_f16(acc + 4 * mt, bf16x2_f16x2(x0.x), bf16x2_f16x2(x8.x), bf16x2_f16x2(x0.y),
+                        bf16x2_f16x2(x8.y), f.x, f.y);
+                mma_f16(acc + 4 * mt, bf16x2_f16x2(x0.z), bf16x2_f16x2(x8.z), bf16x2_f16x2(x0.w),
+                        bf16x2_f16x2(x8.w), f.z, f.w);
+            }
         }
     }
 }
 
-// one 128-row x 32-column fp32 tile with FFMA (tiny fp32 models)
-__device__ __forceinline__ void tile_f32(const Ctx &c, const DMat &d, int slot, int kc,
-                                         float *acc) {
+// one 256-row x 32-column fp32 tile with FFMA (tiny fp32 models): lane l of
+// warp w owns row 32w + l
+__device__ __forceinline__ void tile_f32(const Ctx &c, int K, int slot, int kc, float *acc) {
     const uint32_t tile = sa(c.sm + SM_RING + slot * MK_SLOT);
     const float *act = reinterpret_cast<const float *>(c.sm + SM_SCRATCH);
-    const int row = c.warp * 16 + (c.lane & 15), hf = c.lane >> 4;
-    const int K = d.cols;
+    const int row = c.warp * 32 + c.lane;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint4 w = lds128(tile + row * 128 + (((4 * hf + i) ^ (row & 7)) << 4));
+    for (int i = 0; i < 8; ++i) {
+        uint4 w = lds128(tile + row * 128 + ((i ^ (row & 7)) << 4));
         float wv[4] = {__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
                        __uint_as_float(w.w)};
-        int col = kc * 32 + 16 * hf + 4 * i;
+        int col = kc * 32 + 4 * i;
 #pragma unroll
         for (int t = 0; t < MK_MAXT; ++t) {
             if (t < c.T) {
@@ -683,90 +983,131 @@ __device__ __forceinline__ void tile_f32(const Ctx &c, const DMat &d, int slot, 
 }
 
 // h_e = silu(a/rms) * (b/rms) fragments of one expert (or the shared one)
-__device__ void build_h_frags(const Ctx &c, const RouteSm *rt, int ex, bool f32path) {
+__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + expf(-a)) * b; }
+
+// expert intermediate h = silu(a/rms) * (b/rms) of one routed expert (or the
+// shared one) as f16 fragments; eight blocks of loads are issued at once
+__device__ __noinline__ void build_h_frags(const RouteSm *rt, int ex, bool f32path) {
+    const Ctx c = make_ctx();
     const DModel &m = *c.m;
     const bool shared = ex >= rt->nd;
-    auto hval = [&](int t, int col) -> float {
-        const long long *pa;
-        if (shared) {
-            pa = m.sh_acc + (long long)t * 2 * m.I;
-        } else {
-            int j = rt->dslot[ex][t];
-            if (j < 0) return 0.f;
-            pa = m.ea_acc + (long long)(t * m.K + j) * 2 * m.I;
-        }
-        float inv = c.misc->inv_rms[1][t];
-        float av = from_fx(__ldcg(pa + col)) * inv, bv = from_fx(__ldcg(pa + m.I + col)) * inv;
-        return av / (1.f + expf(-av)) * bv;
+    auto base = [&](int t) -> const long long * {
+        if (t >= c.T) return nullptr;
+        if (shared) return m.sh_acc + (long long)t * 2 * m.I;
+        int j = rt->dslot[ex][t];
+        return j < 0 ? nullptr : m.ea_acc + (long long)(t * m.K + j) * 2 * m.I;
     };
     if (f32path) {
         float *dst = reinterpret_cast<float *>(c.sm + SM_SCRATCH);
         for (int i = c.tid; i < MK_MAXT * m.I; i += MK_NCWARPS * 32) {
             int t = i / m.I, col = i - t * m.I;
-            dst[i] = t < c.T ? hval(t, col) : 0.f;
+            const long long *pa = base(t);
+            float inv = t < c.T ? c.misc->inv_rms[1][t] : 0.f;
+            dst[i] = pa ? silu_mul(from_fx(__ldcg(pa + col)) * inv, from_fx(__ldcg(pa + m.I + col)) * inv) : 0.f;
         }
         return;
     }
-    unsigned char *fr = c.sm + SM_SCRATCH;
     const int s = c.tid >> 5, l = c.lane, n = l >> 2, q = l & 3;
-    for (int kb = 0; kb < m.I / 128; ++kb) {
-        float v[4];
+    const int col0 = frag_col(s, q, 0);
+    const long long *pa = base(n);
+    const float inv = n < c.T ? c.misc->inv_rms[1][n] : 0.f;
+    unsigned char *fr = c.sm + SM_SCRATCH + ((s >> 1) * 32 + l) * 16 + (s & 1) * 8;
+    const int nkb = m.I / 128;
+    for (int kb0 = 0; kb0 < nkb; kb0 += 4) {
+        longlong2 av[4][2], bv[4][2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = n < c.T ? hval(n, kb * 128 + frag_col(s, q, j)) : 0.f;
-        *reinterpret_cast<uint2 *>(fr + kb * 2048 + ((s >> 1) * 32 + l) * 16 + (s & 1) * 8) =
-            make_uint2(pack_f16(v[0], v[1]), pack_f16(v[2], v[3]));
+        for (int i = 0; i < 4; ++i) {
+            if (pa && kb0 + i < nkb) {
+                const longlong2 *pp = reinterpret_cast<const longlong2 *>(pa + (kb0 + i) * 128 + col0);
+                const longlong2 *pb = reinterpret_cast<const longlong2 *>(pa + m.I + (kb0 + i) * 128 + col0);
+                av[i][0] = __ldcg(pp);
+                av[i][1] = __ldcg(pp + 1);
+                bv[i][0] = __ldcg(pb);
+                bv[i][1] = __ldcg(pb + 1);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (kb0 + i >= nkb) break;
+            float h[4] = {0.f, 0.f, 0.f, 0.f};
+            if (pa) {
+                h[0] = silu_mul(from_fx(av[i][0].x) * inv, from_fx(bv[i][0].x) * inv);
+                h[1] = silu_mul(from_fx(av[i][0].y) * inv, from_fx(bv[i][0].y) * inv);
+                h[2] = silu_mul(from_fx(av[i][1].x) * inv, from_fx(bv[i][1].x) * inv);
+                h[3] = silu_mul(from_fx(av[i][1].y) * inv, from_fx(bv[i][1].y) * inv);
+            }
+            *reinterpret_cast<uint2 *>(fr + (kb0 + i) * 2048) =
+                make_uint2(pack_f16(h[0], h[1]), pack_f16(h[2], h[3]));
+        }
     }
 }
 
 // consume this CTA's tiles of one GEMV stage
-__device__ void cons_gemv(Ctx &c, int st, const DLayer &L, const RouteSm *rt, uint32_t &ci) {
-    const DModel &m = *c.m;
-    int b, e;
-    split_range(stage_total(m, st, L, rt), c.G, c.cta, b, e);
+__device__ __forceinline__ void flush_item(const Ctx &c, int st, int ex, int mat, int rg, const MatR &d,
+                                           const RouteSm *rt, const float *acc) {
+    const Tgt g = make_tgt(c, st, ex, mat, d.rows, rt);
+    if (d.dtype == MK_DT_F32) flush_f32(c, g, rg * 256 + c.warp * 32, acc);
+    else flush_mma(c, g, rg * 256 + c.warp * 32, acc);
+}
+
+// consume this CTA's tiles of one GEMV stage
+__device__ __forceinline__ void cons_gemv(const Ctx &c, int st, const DLayer &L, const RouteSm *rt, uint32_t &ci) {
+    StageIter it;
+    stage_iter(it, c, st, L, rt);
+    uint64_t *const full = c.full, *const empty = c.empty;
+    const int lane = c.lane;
     float acc[MK_MAXT];
-    const DMat *cm = nullptr;
-    int ce = -1, crg = -1, cex = -1, cmat = 0, last_hex = -1;
-    Item cur;
-    for (int idx = b; idx < e; ++idx) {
-        Item it = stage_item(m, st, L, rt, idx);
-        const bool f32 = it.m->dtype == MK_DT_F32;
-        if (it.m != cm || it.e != ce || it.rg != crg || it.ex != cex || it.mat != cmat) {
-            if (cm) {
-                Tgt g;
-                make_tgt(c, st, cur, rt, g);
-                if (cm->dtype == MK_DT_F32) flush_f32(c, g, cur.rg * 128 + c.warp * 16, acc);
-                else flush_mma(c, g, cur.rg * 128 + c.warp * 16, acc);
-            }
 #pragma unroll
-            for (int i = 0; i < MK_MAXT; ++i) acc[i] = 0.f;
-            cm = it.m;
-            ce = it.e;
-            crg = it.rg;
+    for (int i = 0; i < MK_MAXT; ++i) acc[i] = 0.f;
+    int cex = -1, cmat = 0, crg = 0, last_hex = -1;
+    const bool prof = c.p->marks != nullptr;
+    unsigned long long cy_wait = 0, cy_comp = 0, cy_other = 0, cy0 = prof ? clock64() : 0;
+    const int ntiles = it.n;
+    for (int k = 0; it.n > 0; --it.n, it.advance(), ++k) {
+        const MatR &d = it.cur();
+        if (k == 0 || it.kc == 0) {  // a new (expert slot, matrix, row group) item starts
+            if (k > 0) {
+                flush_item(c, st, cex, cmat, crg, cmat || (st == ST_EXPB && cex >= it.nd) ? it.m1 : it.m0, rt, acc);
+#pragma unroll
+                for (int i = 0; i < MK_MAXT; ++i) acc[i] = 0.f;
+            }
             cex = it.ex;
             cmat = it.mat;
-            cur = it;
+            crg = it.rg;
             if (st == ST_EXPB && it.ex != last_hex) {
                 bar_consumers();
-                build_h_frags(c, rt, it.ex, f32);
+                build_h_frags(rt, it.ex, d.dtype == MK_DT_F32);
                 bar_consumers();
                 last_hex = it.ex;
             }
         }
         const int slot = ci % MK_RING;
-        if (mbar_wait(&c.full[slot], (ci / MK_RING) & 1, c, 200 + st)) {
-            if (f32) tile_f32(c, *it.m, slot, it.kc, acc);
-            else tile_mma(c, *it.m, slot, it.kc, acc);
+        unsigned long long cy1 = prof ? clock64() : 0;
+        if (mbar_wait(&full[slot], (ci / MK_RING) & 1, c, 200 + st)) {
+            unsigned long long cy2 = prof ? clock64() : 0;
+            if (k == 0) mark(c, st * 16 + 1);
+            if (d.dtype == MK_DT_F32) tile_f32(c, d.cols, slot, it.kc, acc);
+            else tile_mma(c, d.dtype, slot, it.kc, acc);
+            if (prof) {
+                unsigned long long cy3 = clock64();
+                cy_wait += cy2 - cy1;
+                cy_comp += cy3 - cy2;
+                cy_other += cy1 - cy0;
+                cy0 = cy3;
+            }
         }
         __syncwarp();
-        if (c.lane == 0) mbar_arrive(&c.empty[slot]);
+        if (lane == 0) mbar_arrive(&empty[slot]);
         ++ci;
     }
-    if (cm) {
-        Tgt g;
-        make_tgt(c, st, cur, rt, g);
-        if (cm->dtype == MK_DT_F32) flush_f32(c, g, cur.rg * 128 + c.warp * 16, acc);
-        else flush_mma(c, g, cur.rg * 128 + c.warp * 16, acc);
+    if (ntiles > 0)
+        flush_item(c, st, cex, cmat, crg, cmat || (st == ST_EXPB && cex >= it.nd) ? it.m1 : it.m0, rt, acc);
+    if (prof && c.lane == 0 && c.warp == 0) {
+        mark_val(c, MK_MARKS - 64 + st * 4 + 0, 900 + st * 4 + 0, cy_wait);
+        mark_val(c, MK_MARKS - 64 + st * 4 + 1, 900 + st * 4 + 1, cy_comp);
+        mark_val(c, MK_MARKS - 64 + st * 4 + 2, 900 + st * 4 + 2, cy_other);
     }
+    mark(c, st * 16 + 2);
 }
 
 // ------------------------------------------------------------------ small helpers
@@ -792,10 +1133,12 @@ __device__ void ssq_block(const Ctx &c, int which) {
 }
 __device__ void compute_inv_rms(const Ctx &c, int which) {
     const DModel &m = *c.m;
-    if (c.tid < c.T) {
-        float s = 0.f;
-        for (int kb = 0; kb < m.H / 128; ++kb) s += __ldcg(m.ssq + (which * MK_MAXKB + kb) * MK_MAXT + c.tid);
-        c.misc->inv_rms[which][c.tid] = rsqrtf(s / (float)m.H + m.eps);
+    if (c.warp < c.T) {
+        const int t = c.warp;
+        float v = c.lane < m.H / 128 ? __ldcg(m.ssq + (which * MK_MAXKB + c.lane) * MK_MAXT + t) : 0.f;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (c.lane == 0) c.misc->inv_rms[which][t] = rsqrtf(v / (float)m.H + m.eps);
     }
 }
 
@@ -827,21 +1170,41 @@ __device__ __forceinline__ void bitonic16_desc(unsigned long long *v) {
 }
 
 // top-K of each token's sigmoid scores + bias; weights from the unbiased scores
-__device__ void route_layer(Ctx &c, const DLayer &L, RouteSm *rt) {
+__device__ __noinline__ void route_layer(const DLayer *Lp, RouteSm *rt) {
+    const Ctx c = make_ctx();
+    const DLayer &L = *Lp;
     const DModel &m = *c.m;
+    mark(c, ST_EXPA * 16 + 4);
     if (c.warp < c.T) {
         const int t = c.warp;
         const float inv = c.misc->inv_rms[1][t];
         unsigned long long v[16];
+        long long raw[16];
+        float bias[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {  // phase 1: all loads in flight
+            int e = c.lane + 32 * i;
+            raw[i] = 0;
+            bias[i] = 0.f;
+            if (e < m.E) {
+                raw[i] = __ldcg(m.rlog + (long long)t * m.E + e);
+                bias[i] = __ldg(L.router_bias + e);
+            }
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             int e = c.lane + 32 * i;
             v[i] = 0ull;
             if (e < m.E) {
-                float lg = from_fx(__ldcg(m.rlog + (long long)t * m.E + e)) * inv;
+                float lg = from_fx(raw[i]) * inv;
                 float s = 1.f / (1.f + expf(-lg));
-                v[i] = key64(s + __ldg(L.router_bias + e), e);
+                v[i] = key64(s + bias[i], e);
             }
+        }
+        if (c.warp == 0 && c.lane == 0 && c.p->marks) {
+            unsigned long long *e = c.p->marks + ((long long)c.cta * MK_MARKS + (MK_MARKS - 72)) * 2;
+            e[0] = ST_EXPA * 16 + 5;
+            e[1] = gtimer();
         }
         bitonic16_desc(v);
         // bitonic merge of the lanes' sorted top-8 lists
@@ -885,6 +1248,7 @@ __device__ void route_layer(Ctx &c, const DLayer &L, RouteSm *rt) {
     }
     if (c.tid < 16) c.misc->emask[c.tid] = 0;
     bar_consumers();
+    mark(c, ST_EXPA * 16 + 6);
     if (c.warp == 0) {
         for (int i = c.lane; i < c.T * m.K; i += 32) {
             int e = rt->idx[i / m.K][i % m.K];
@@ -935,21 +1299,51 @@ __device__ void att_prepare(const Ctx &c, int l, const AttUnit &u, bool mma_path
     const DModel &m = *c.m;
     const int G = m.Hq / m.Hkv, R = G * c.T, hd = m.d / 2;
     unsigned char *scr = c.sm + SM_SCRATCH;
-    // rotated queries
-    for (int i = c.tid; i < R * hd; i += MK_NCWARPS * 32) {
-        int row = i / hd, k = i - row * hd;
-        int t = row / G, h = u.g * G + (row - t * G);
-        float x1 = qkv_val(c, t, h * m.d + k), x2 = qkv_val(c, t, h * m.d + k + hd);
-        float2 cs = __ldg(m.rope + (long long)(c.ctx + t) * hd + k);
-        float y1 = x1 * cs.x - x2 * cs.y, y2 = x2 * cs.x + x1 * cs.y;
-        if (mma_path) {
-            __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(scr);
-            qs[row * 136 + k] = __float2bfloat16_rn(y1);
-            qs[row * 136 + k + hd] = __float2bfloat16_rn(y2);
-        } else {
-            float *qs = reinterpret_cast<float *>(scr);
-            qs[row * m.d + k] = y1;
-            qs[row * m.d + k + hd] = y2;
+    // rotated queries: 4 consecutive pairs per item, loads of 4 items in flight
+    const int nk4 = hd / 4, nitem = R * nk4;
+    for (int i0 = c.tid; i0 < nitem; i0 += 2 * MK_NCWARPS * 32) {
+        longlong2 xa[2][2], xb[2][2];
+        float4 ra[2][2];
+#pragma unroll
+        for (int u4 = 0; u4 < 2; ++u4) {
+            int i = i0 + u4 * MK_NCWARPS * 32;
+            if (i < nitem) {
+                int row = i / nk4, k = (i - row * nk4) * 4;
+                int t = row / G, h = u.g * G + (row - t * G);
+                const long long *b = m.qkv_acc + (long long)t * m.nqkv + h * m.d + k;
+                xa[u4][0] = __ldcg(reinterpret_cast<const longlong2 *>(b));
+                xa[u4][1] = __ldcg(reinterpret_cast<const longlong2 *>(b) + 1);
+                xb[u4][0] = __ldcg(reinterpret_cast<const longlong2 *>(b + hd));
+                xb[u4][1] = __ldcg(reinterpret_cast<const longlong2 *>(b + hd) + 1);
+                const float4 *rp = reinterpret_cast<const float4 *>(m.rope + (long long)(c.ctx + t) * hd + k);
+                ra[u4][0] = __ldg(rp);
+                ra[u4][1] = __ldg(rp + 1);
+            }
+        }
+#pragma unroll
+        for (int u4 = 0; u4 < 2; ++u4) {
+            int i = i0 + u4 * MK_NCWARPS * 32;
+            if (i >= nitem) break;
+            int row = i / nk4, k = (i - row * nk4) * 4;
+            float inv = c.misc->inv_rms[0][row / G];
+            float x1[4] = {from_fx(xa[u4][0].x), from_fx(xa[u4][0].y), from_fx(xa[u4][1].x), from_fx(xa[u4][1].y)};
+            float x2[4] = {from_fx(xb[u4][0].x), from_fx(xb[u4][0].y), from_fx(xb[u4][1].x), from_fx(xb[u4][1].y)};
+            float cs[8] = {ra[u4][0].x, ra[u4][0].y, ra[u4][0].z, ra[u4][0].w,
+                           ra[u4][1].x, ra[u4][1].y, ra[u4][1].z, ra[u4][1].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float a1 = x1[j] * inv, a2 = x2[j] * inv;
+                float y1 = a1 * cs[2 * j] - a2 * cs[2 * j + 1], y2 = a2 * cs[2 * j] + a1 * cs[2 * j + 1];
+                if (mma_path) {
+                    __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(scr);
+                    qs[row * 136 + k + j] = __float2bfloat16_rn(y1);
+                    qs[row * 136 + k + j + hd] = __float2bfloat16_rn(y2);
+                } else {
+                    float *qs = reinterpret_cast<float *>(scr);
+                    qs[row * m.d + k + j] = y1;
+                    qs[row * m.d + k + j + hd] = y2;
+                }
+            }
         }
     }
     if (mma_path) {  // zero the padding rows of the last m-tile
@@ -1020,105 +1414,106 @@ __device__ void att_prepare(const Ctx &c, int l, const AttUnit &u, bool mma_path
 
 // tensor-core attention state of one warp (16 query rows, d = 128)
 struct AttMma {
-    uint32_t qf[8][4];
+    uint32_t qaddr;       // ldmatrix row address of this lane in the rotated queries
     float o[16][4];
     float mrow[2], lrow[2];
 };
 
-// one key page: kbase/vbase hold [2 boxes][nkeys][128 B] swizzled, box stride bs
+// one key page of nkeys (64, or 16 for the block's own keys): kbase/vbase hold
+// [2 boxes][nkeys][128 B] swizzled with box stride bs.  Keys are taken in
+// 32-key halves, each with its own online-softmax update.
 __device__ void att_page_mma(const Ctx &c, AttMma &A, uint32_t kbase, uint32_t vbase, int bs,
-                             int nnt, int key_base, int valid, bool causal, int mt, int G) {
-    const int r = c.lane >> 2, q = c.lane & 3;
+                             int nkeys, int valid, bool causal, int mt, int G) {
+    const int r = c.lane >> 2, q = c.lane & 3, mi = c.lane >> 3, li = c.lane & 7;
     const float sl2 = rsqrtf((float)c.m->d) * 1.4426950408889634f;
-    float sc[8][4];
+    for (int h0 = 0; h0 < nkeys; h0 += 32) {
+        const int nnt = min(4, (nkeys - h0) >> 3);
+        float sc[4][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-        if (nt < nnt) {
+        for (int i = 0; i < 4; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
 #pragma unroll
-            for (int kk2 = 0; kk2 < 4; ++kk2) {
-                int key = 8 * nt + (c.lane & 7);
-                int dch = 4 * kk2 + (c.lane >> 3);
-                uint32_t ad = kbase + (dch >> 3) * bs + key * 128 + (((dch & 7) ^ (key & 7)) << 4);
-                uint32_t b0, b1, b2, b3;
-                ldsm4(ad, b0, b1, b2, b3);
-                mma_bf16(sc[nt], A.qf[2 * kk2][0], A.qf[2 * kk2][1], A.qf[2 * kk2][2], A.qf[2 * kk2][3], b0, b1);
-                mma_bf16(sc[nt], A.qf[2 * kk2 + 1][0], A.qf[2 * kk2 + 1][1], A.qf[2 * kk2 + 1][2],
-                         A.qf[2 * kk2 + 1][3], b2, b3);
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t q0, q1, q2, q3;  // query fragment of head dims 16kk..16kk+15
+            ldsm4(A.qaddr + kk * 32, q0, q1, q2, q3);
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+                if (2 * pp < nnt) {
+                    int key = h0 + 8 * (2 * pp + (mi >> 1)) + li;
+                    int dch = 2 * kk + (mi & 1);
+                    uint32_t ad = kbase + (dch >> 3) * bs + key * 128 + (((dch & 7) ^ (key & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm4(ad, b0, b1, b2, b3);
+                    mma_bf16(sc[2 * pp], q0, q1, q2, q3, b0, b1);
+                    mma_bf16(sc[2 * pp + 1], q0, q1, q2, q3, b2, b3);
+                }
             }
         }
-    }
-    // mask, scale, online softmax (log2 domain)
-    float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
+        // mask, scale, online softmax (log2 domain)
+        float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+        for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            int key = 8 * nt + 2 * q + (i & 1);
-            int row = mt * 16 + r + (i >> 1) * 8;
-            bool ok = nt < nnt && key < valid;
-            if (causal) ok = ok && key <= row / G;
-            float v = ok ? sc[nt][i] * sl2 : -CUDART_INF_F;
-            sc[nt][i] = v;
-            mx[i >> 1] = fmaxf(mx[i >> 1], v);
+            for (int i = 0; i < 4; ++i) {
+                int key = h0 + 8 * nt + 2 * q + (i & 1);
+                int row = mt * 16 + r + (i >> 1) * 8;
+                bool ok = nt < nnt && key < valid;
+                if (causal) ok = ok && key <= row / G;
+                float v = ok ? sc[nt][i] * sl2 : -CUDART_INF_F;
+                sc[nt][i] = v;
+                mx[i >> 1] = fmaxf(mx[i >> 1], v);
+            }
         }
-    }
+        float corr[2], mn[2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-    }
-    float corr[2], mn[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        mn[h] = fmaxf(A.mrow[h], mx[h]);
-        corr[h] = exp2f(A.mrow[h] - mn[h]);
-        A.mrow[h] = mn[h];
-        A.lrow[h] *= corr[h];
-    }
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float p = exp2f(sc[nt][i] - mn[i >> 1]);
-            sc[nt][i] = p;
-            A.lrow[i >> 1] += p;
+        for (int h = 0; h < 2; ++h) {
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+            mn[h] = fmaxf(A.mrow[h], mx[h]);
+            corr[h] = exp2f(A.mrow[h] - mn[h]);
+            A.mrow[h] = mn[h];
+            A.lrow[h] *= corr[h];
         }
-    }
 #pragma unroll
-    for (int nd = 0; nd < 16; ++nd) {
-        A.o[nd][0] *= corr[0];
-        A.o[nd][1] *= corr[0];
-        A.o[nd][2] *= corr[1];
-        A.o[nd][3] *= corr[1];
-    }
-    // P V
-    const bool partial = valid < 8 * nnt;
+        for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
-    for (int kk2 = 0; kk2 < 4; ++kk2) {
-        if (2 * kk2 < nnt) {
-            uint32_t a0 = pack_bf16(sc[2 * kk2][0], sc[2 * kk2][1]);
-            uint32_t a1 = pack_bf16(sc[2 * kk2][2], sc[2 * kk2][3]);
-            uint32_t a2 = pack_bf16(sc[2 * kk2 + 1][0], sc[2 * kk2 + 1][1]);
-            uint32_t a3 = pack_bf16(sc[2 * kk2 + 1][2], sc[2 * kk2 + 1][3]);
-            const int klo = 16 * kk2 + 2 * q;  // keys of b0/b2 halves: klo, klo+1; b1/b3: klo+8, +9
+            for (int i = 0; i < 4; ++i) {
+                float pv = exp2f(sc[nt][i] - mn[i >> 1]);
+                sc[nt][i] = pv;
+                A.lrow[i >> 1] += pv;
+            }
+        }
 #pragma unroll
-            for (int np = 0; np < 8; ++np) {
-                int key = 16 * kk2 + (c.lane & 7) + ((c.lane >> 3) & 1) * 8;
-                int dch = 2 * np + (c.lane >> 4);
-                uint32_t ad = vbase + (dch >> 3) * bs + key * 128 + (((dch & 7) ^ (key & 7)) << 4);
-                uint32_t b0, b1, b2, b3;
-                ldsm4t(ad, b0, b1, b2, b3);
+        for (int nd = 0; nd < 16; ++nd) {
+            A.o[nd][0] *= corr[0];
+            A.o[nd][1] *= corr[0];
+            A.o[nd][2] *= corr[1];
+            A.o[nd][3] *= corr[1];
+        }
+        // P V over the half's 16-key steps
+        const bool partial = valid < h0 + 8 * nnt;
+#pragma unroll
+        for (int kk2 = 0; kk2 < 2; ++kk2) {
+            if (2 * kk2 < nnt) {
+                uint32_t a0 = pack_bf16(sc[2 * kk2][0], sc[2 * kk2][1]);
+                uint32_t a1 = pack_bf16(sc[2 * kk2][2], sc[2 * kk2][3]);
+                uint32_t a2 = pack_bf16(sc[2 * kk2 + 1][0], sc[2 * kk2 + 1][1]);
+                uint32_t a3 = pack_bf16(sc[2 * kk2 + 1][2], sc[2 * kk2 + 1][3]);
+                const int klo = h0 + 16 * kk2 + 2 * q;
+                uint32_t m0 = 0xffffffffu, m1 = 0xffffffffu;
                 if (partial) {
-                    uint32_t m0 = (klo < valid ? 0xffffu : 0u) | (klo + 1 < valid ? 0xffff0000u : 0u);
-                    uint32_t m1 = (klo + 8 < valid ? 0xffffu : 0u) | (klo + 9 < valid ? 0xffff0000u : 0u);
-                    b0 &= m0;
-                    b2 &= m0;
-                    b1 &= m1;
-                    b3 &= m1;
+                    m0 = (klo < valid ? 0xffffu : 0u) | (klo + 1 < valid ? 0xffff0000u : 0u);
+                    m1 = (klo + 8 < valid ? 0xffffu : 0u) | (klo + 9 < valid ? 0xffff0000u : 0u);
                 }
-                mma_bf16(A.o[2 * np], a0, a1, a2, a3, b0, b1);
-                mma_bf16(A.o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+#pragma unroll
+                for (int np = 0; np < 8; ++np) {
+                    int key = h0 + 16 * kk2 + li + (mi & 1) * 8;
+                    int dch = 2 * np + (mi >> 1);
+                    uint32_t ad = vbase + (dch >> 3) * bs + key * 128 + (((dch & 7) ^ (key & 7)) << 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm4t(ad, b0, b1, b2, b3);
+                    mma_bf16(A.o[2 * np], a0, a1, a2, a3, b0 & m0, b1 & m1);
+                    mma_bf16(A.o[2 * np + 1], a0, a1, a2, a3, b2 & m0, b3 & m1);
+                }
             }
         }
     }
@@ -1126,20 +1521,20 @@ __device__ void att_page_mma(const Ctx &c, AttMma &A, uint32_t kbase, uint32_t v
 
 // FFMA attention of one page for <= 16 rows (fp32 caches, head_dim 64)
 struct AttF {
-    float o[16][4];
+    float o[16][2];
     float mrow[16], lrow[16];
 };
 __device__ void att_page_f32(const Ctx &c, AttF &A, const float *qs, int R, int G,
                              const unsigned char *kb, const unsigned char *vb, int bs, int es,
                              bool plain, int key0, int nkeys, int valid, bool causal) {
     const DModel &m = *c.m;
-    const int nd = m.d / 32;
+    const int nd = 2;  // head_dim 64
     const float sl2 = rsqrtf((float)m.d) * 1.4426950408889634f;
     for (int key = key0; key < key0 + nkeys; ++key) {
         if (key >= valid) break;
-        float kv[4], vv[4];
+        float kv[2], vv[2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             kv[i] = vv[i] = 0.f;
             if (i < nd) {
                 int dd = c.lane + 32 * i;
@@ -1164,8 +1559,7 @@ __device__ void att_page_f32(const Ctx &c, AttF &A, const float *qs, int R, int 
             if (rr < R) {
                 float s = 0.f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (i < nd) s += qs[rr * m.d + c.lane + 32 * i] * kv[i];
+                for (int i = 0; i < 2; ++i) s += qs[rr * m.d + c.lane + 32 * i] * kv[i];
 #pragma unroll
                 for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                 if (causal && key > rr / G) continue;
@@ -1175,13 +1569,15 @@ __device__ void att_page_f32(const Ctx &c, AttF &A, const float *qs, int R, int 
                 A.mrow[rr] = mn;
                 A.lrow[rr] = A.lrow[rr] * corr + p;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) A.o[rr][i] = A.o[rr][i] * corr + p * vv[i];
+                for (int i = 0; i < 2; ++i) A.o[rr][i] = A.o[rr][i] * corr + p * vv[i];
             }
         }
     }
 }
 
-__device__ bool cons_att(Ctx &c, int l, uint32_t &ci) {
+// returns the ring position after this CTA's pages, or -1 if the step aborted
+__device__ __noinline__ long long cons_att(int l, uint32_t ci) {
+    const Ctx c = make_ctx();
     const DModel &m = *c.m;
     const AttUnit u = att_unit(c);
     const int G = m.Hq / m.Hkv, R = G * c.T;
@@ -1192,6 +1588,7 @@ __device__ bool cons_att(Ctx &c, int l, uint32_t &ci) {
     bar_consumers();
     if (u.active) att_prepare(c, l, u, mma_path);
     bar_consumers();
+    mark(c, ST_ATT * 16 + 0);
     unsigned char *scr = c.sm + SM_SCRATCH;
     float *part = m.att_part + (long long)(u.g * MK_MAXSPLIT + u.s) * MK_MAXROWS * D2;
     if (u.active && mma_path) {
@@ -1203,34 +1600,25 @@ __device__ bool cons_att(Ctx &c, int l, uint32_t &ci) {
         A.lrow[0] = A.lrow[1] = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) A.o[i][0] = A.o[i][1] = A.o[i][2] = A.o[i][3] = 0.f;
-        if (wact) {
-            const uint32_t qs = sa(scr);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                int row = mt * 16 + (c.lane & 7) + ((c.lane >> 3) & 1) * 8;
-                int col = 16 * kk + (c.lane >> 4) * 8;
-                ldsm4(qs + row * 272 + col * 2, A.qf[kk][0], A.qf[kk][1], A.qf[kk][2], A.qf[kk][3]);
-            }
+        {
+            int row = mt * 16 + (c.lane & 7) + ((c.lane >> 3) & 1) * 8;
+            A.qaddr = sa(scr) + row * 272 + (c.lane >> 4) * 16;
         }
         for (int j = u.p0; j < u.pc1; ++j) {
-            const int ks = ci % MK_RING, vs = (ci + 1) % MK_RING;
+            const int ks = ci % MK_RING;
             bool ok = mbar_wait(&c.full[ks], (ci / MK_RING) & 1, c, 210);
-            ok = mbar_wait(&c.full[vs], ((ci + 1) / MK_RING) & 1, c, 211) && ok;
             if (ok && wact && ((j - u.p0) % nws) == ws) {
                 int valid = min(m.P, c.ctx - j * m.P);
-                att_page_mma(c, A, sa(c.sm + SM_RING + ks * MK_SLOT), sa(c.sm + SM_RING + vs * MK_SLOT),
-                             bs, 8, j * m.P, valid, false, mt, G);
+                const uint32_t kb = sa(c.sm + SM_RING + ks * MK_SLOT);
+                att_page_mma(c, A, kb, kb + MK_SLOT / 2, bs, 64, valid, false, mt, G);
             }
             __syncwarp();
-            if (c.lane == 0) {
-                mbar_arrive(&c.empty[ks]);
-                mbar_arrive(&c.empty[vs]);
-            }
-            ci += 2;
+            if (c.lane == 0) mbar_arrive(&c.empty[ks]);
+            ci += 1;
         }
         if (u.has_new && wact && ((u.pc1 - u.p0) % nws) == ws) {
             uint32_t mini = sa(scr + 17408);
-            att_page_mma(c, A, mini, mini + 4096, 2048, 2, 0, c.T, true, mt, G);
+            att_page_mma(c, A, mini, mini + 4096, 2048, 16, c.T, true, mt, G);
         }
         // finish row sums
 #pragma unroll
@@ -1301,25 +1689,22 @@ __device__ bool cons_att(Ctx &c, int l, uint32_t &ci) {
         for (int rr = 0; rr < 16; ++rr) {
             A.mrow[rr] = -1e30f;
             A.lrow[rr] = 0.f;
-            A.o[rr][0] = A.o[rr][1] = A.o[rr][2] = A.o[rr][3] = 0.f;
+            A.o[rr][0] = A.o[rr][1] = 0.f;
         }
         const float *qs = reinterpret_cast<const float *>(scr);
         const int kpw = m.P / MK_NCWARPS;
         for (int j = u.p0; j < u.pc1; ++j) {
-            const int ks = ci % MK_RING, vs = (ci + 1) % MK_RING;
+            const int ks = ci % MK_RING;
             bool ok = mbar_wait(&c.full[ks], (ci / MK_RING) & 1, c, 212);
-            ok = mbar_wait(&c.full[vs], ((ci + 1) / MK_RING) & 1, c, 213) && ok;
             if (ok) {
                 int valid = min(m.P, c.ctx - j * m.P);
-                att_page_f32(c, A, qs, R, G, c.sm + SM_RING + ks * MK_SLOT, c.sm + SM_RING + vs * MK_SLOT,
-                             bs, m.kv_es, false, c.warp * kpw, kpw, valid, false);
+                unsigned char *kb = c.sm + SM_RING + ks * MK_SLOT;
+                att_page_f32(c, A, qs, R, G, kb, kb + MK_SLOT / 2, bs, m.kv_es, false, c.warp * kpw, kpw,
+                             valid, false);
             }
             __syncwarp();
-            if (c.lane == 0) {
-                mbar_arrive(&c.empty[ks]);
-                mbar_arrive(&c.empty[vs]);
-            }
-            ci += 2;
+            if (c.lane == 0) mbar_arrive(&c.empty[ks]);
+            ci += 1;
         }
         if (u.has_new && c.warp == 0) {
             const unsigned char *mini = scr + 17408;
@@ -1334,8 +1719,7 @@ __device__ bool cons_att(Ctx &c, int l, uint32_t &ci) {
         for (int rr = 0; rr < 16; ++rr) {
             if (rr < R) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (i < nd) w[rr * m.d + c.lane + 32 * i] = A.o[rr][i];
+                for (int i = 0; i < 2; ++i) w[rr * m.d + c.lane + 32 * i] = A.o[rr][i];
                 if (c.lane == 0) {
                     w[MO + rr] = A.mrow[rr];
                     w[MO + 16 + rr] = A.lrow[rr];
@@ -1363,7 +1747,8 @@ __device__ bool cons_att(Ctx &c, int l, uint32_t &ci) {
     }
     // group barrier among the splits of this kv head, then merge assigned rows
     bar_consumers();
-    if (!u.active) return true;
+    mark(c, ST_ATT * 16 + 1);
+    if (!u.active) return ci;
     if (c.tid == 0) {
         bool ok = !aborted(c);
         __threadfence();
@@ -1373,29 +1758,66 @@ __device__ bool cons_att(Ctx &c, int l, uint32_t &ci) {
         c.misc->gs_ok = ok;
     }
     bar_consumers();
-    if (!c.misc->gs_ok) return false;
+    mark(c, ST_ATT * 16 + 2);
+    if (!c.misc->gs_ok) return -1;
     int r0, r1;
     split_range(R, c.nsplit, u.s, r0, r1);
+    const int nr = r1 - r0, ns = c.nsplit;
     const float *pbase = m.att_part + (long long)(u.g * MK_MAXSPLIT) * MK_MAXROWS * D2;
-    for (int i = c.tid; i < (r1 - r0) * m.d; i += MK_NCWARPS * 32) {
-        int row = r0 + i / m.d, dd = i % m.d;
-        float mn = -1e30f;
-        for (int s = 0; s < c.nsplit; ++s) mn = fmaxf(mn, __ldcg(pbase + ((long long)s * MK_MAXROWS + row) * D2 + m.d));
-        float acc = 0.f, lsum = 0.f;
-        for (int s = 0; s < c.nsplit; ++s) {
-            const float *pp = pbase + ((long long)s * MK_MAXROWS + row) * D2;
-            float a = exp2f(__ldcg(pp + m.d) - mn);
-            acc += a * __ldcg(pp + dd);
-            lsum += a * __ldcg(pp + m.d + 1);
-        }
-        int t = row / G, h = u.g * G + (row - t * G);
-        __stcg(m.o_buf + (long long)t * m.Hq * m.d + h * m.d + dd, acc / lsum);
+    // per-split weights exp2(m_s - M) / L of my rows, in scratch
+    float *wts = reinterpret_cast<float *>(scr);            // [nr][ns]
+    for (int i = c.tid; i < nr * ns; i += MK_NCWARPS * 32) {
+        int rr = i / ns, sp = i - rr * ns;
+        const float *pp = pbase + ((long long)sp * MK_MAXROWS + r0 + rr) * D2 + m.d;
+        wts[i] = __ldcg(pp);                                 // m
+        wts[nr * ns + i] = __ldcg(pp + 1);                   // l
     }
-    return true;
+    bar_consumers();
+    if (c.tid < nr) {
+        float *mw = wts + c.tid * ns, *lw = wts + nr * ns + c.tid * ns;
+        float mx = -1e30f;
+        for (int sp = 0; sp < ns; ++sp) mx = fmaxf(mx, mw[sp]);
+        float lsum = 0.f;
+        for (int sp = 0; sp < ns; ++sp) {
+            float a = exp2f(mw[sp] - mx);
+            mw[sp] = a;
+            lsum += a * lw[sp];
+        }
+        float il = 1.f / lsum;
+        for (int sp = 0; sp < ns; ++sp) mw[sp] *= il;
+    }
+    bar_consumers();
+    for (int i = c.tid; i < nr * m.d; i += MK_NCWARPS * 32) {
+        int rr = i / m.d, dd = i - rr * m.d;
+        const float *w = wts + rr * ns;
+        const float *pp = pbase + (long long)(r0 + rr) * D2 + dd;
+        float acc = 0.f;
+        int sp = 0;
+        for (; sp + 8 <= ns; sp += 8) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = __ldcg(pp + (long long)(sp + k) * MK_MAXROWS * D2);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc += w[sp + k] * v[k];
+        }
+        for (; sp < ns; ++sp) acc += w[sp] * __ldcg(pp + (long long)sp * MK_MAXROWS * D2);
+        int row = r0 + rr, t = row / G, h = u.g * G + (row - t * G);
+        __stcg(m.o_buf + (long long)t * m.Hq * m.d + h * m.d + dd, acc);
+    }
+    mark(c, ST_ATT * 16 + 3);
+    return ci;
 }
 
 // ------------------------------------------------------------------ consumer
-__device__ void consumer(Ctx &c) {
+// copy one layer's descriptors into shared memory (consumer threads)
+__device__ __forceinline__ void copy_layer(const Ctx &c, DLayer *dst, const DLayer *src) {
+    const int nw = (int)(sizeof(DLayer) / 4);
+    for (int i = c.tid; i < nw; i += MK_NCWARPS * 32)
+        reinterpret_cast<uint32_t *>(dst)[i] = __ldg(reinterpret_cast<const uint32_t *>(src) + i);
+}
+
+__device__ __noinline__ void consumer() {
+    const Ctx c = make_ctx();
     const DModel &m = *c.m;
     const Params &p = *c.p;
     uint32_t ci = 0;
@@ -1423,52 +1845,64 @@ __device__ void consumer(Ctx &c) {
     if (!grid_sync(c, 1)) return;
     for (int li = 0; li < nl; ++li) {
         const int l = p.mode ? p.layer : li;
-        const DLayer &L = m.layers[l];
+        const DLayer &L = c.misc->L[li & 1];
         RouteSm *rt = &c.rt[li & 1];
+        // descriptors of the next layer, read by the producer once it gets there
+        // (it cannot pass this layer's tiles before these stores are done)
+        if (p.mode == 0 && li + 1 < nl) copy_layer(c, &c.misc->L[(li + 1) & 1], m.layers + li + 1);
         // ---- QKV
         {
             ActSrc a{m.res, nullptr, m.H, L.attn_norm};
             int b, e;
             split_range(stage_total(m, ST_QKV, L, rt), c.G, c.cta, b, e);
-            if (f32path) build_act32(c, a, m.H);
-            else build_frags(c, a, needed_kb(b, e, L.qkv));
+            if (f32path) build_act32(a, m.H);
+            else build_frags(a, needed_kb(b, e, L.qkv));
             ssq_block(c, 0);
             zero_slice(c, m.sh_acc, (long long)MK_MAXT * 2 * m.I);
             zero_slice(c, m.ea_acc, (long long)MK_MAXT * m.K * 2 * m.I);
             bar_consumers();
+            mark(c, ST_QKV * 16 + 0);
             cons_gemv(c, ST_QKV, L, rt, ci);
             if (!grid_sync(c, 2)) return;
         }
         // ---- attention
-        if (!cons_att(c, l, ci)) return;
+        {
+            const long long r = cons_att(l, ci);
+            if (r < 0) return;
+            ci = (uint32_t)r;
+        }
         if (!grid_sync(c, 3)) return;
         // ---- O projection (+ residual)
         {
             ActSrc a{nullptr, m.o_buf, m.Hq * m.d, nullptr};
             int b, e;
             split_range(stage_total(m, ST_O, L, rt), c.G, c.cta, b, e);
-            if (f32path) build_act32(c, a, m.Hq * m.d);
-            else build_frags(c, a, needed_kb(b, e, L.o));
+            if (f32path) build_act32(a, m.Hq * m.d);
+            else build_frags(a, needed_kb(b, e, L.o));
             zero_slice(c, m.qkv_acc, (long long)MK_MAXT * m.nqkv);
             bar_consumers();
+            mark(c, ST_O * 16 + 0);
             cons_gemv(c, ST_O, L, rt, ci);
             if (!grid_sync(c, 4)) return;
         }
         // ---- router + shared expert gate/up, then routed gate/up
         {
             ActSrc a{m.res, nullptr, m.H, L.moe_norm};
-            if (f32path) build_act32(c, a, m.H);
-            else build_frags(c, a, allH);
+            if (f32path) build_act32(a, m.H);
+            else build_frags(a, allH);
             ssq_block(c, 1);
             bar_consumers();
+            mark(c, ST_ROUTER * 16 + 0);
             cons_gemv(c, ST_ROUTER, L, rt, ci);
             grid_arrive(c);
             cons_gemv(c, ST_SHA, L, rt, ci);
             if (!grid_wait(c, 5)) return;
             compute_inv_rms(c, 1);
             bar_consumers();
-            route_layer(c, L, rt);
+            mark(c, ST_EXPA * 16 + 3);
+            route_layer(&L, rt);
             if (c.tid == 0) mbar_arrive(c.route);
+            mark(c, ST_EXPA * 16 + 0);
             if (c.cta == 0) {
                 if (c.tid == 0) c.misc->distinct_total += rt->nd;
                 if (p.mode == 1) {
@@ -1486,6 +1920,7 @@ __device__ void consumer(Ctx &c) {
         }
         // ---- routed + shared down projections (+ residual)
         zero_slice(c, m.rlog, (long long)MK_MAXT * m.E);
+        mark(c, ST_EXPB * 16 + 0);
         cons_gemv(c, ST_EXPB, L, rt, ci);
         if (!grid_sync(c, 7)) return;
     }
@@ -1493,16 +1928,16 @@ __device__ void consumer(Ctx &c) {
         long long n = (long long)c.T * m.H;
         long long b = n * c.cta / c.G, e = n * (c.cta + 1) / c.G;
         for (long long i = b + c.tid; i < e; i += MK_NCWARPS * 32) p.hidden_out[i] = from_fx(__ldcg(m.res + i));
-        if (c.cta == 0 && c.tid == 0) c.ctrl->epoch = c.bar_base + (unsigned long long)c.nbar * c.G;
+        if (c.cta == 0 && c.tid == 0) c.ctrl->epoch = c.misc->base + (unsigned long long)c.misc->nbar * c.G;
         return;
     }
     // ---- final norm + LM head
     {
         ActSrc a{m.res, nullptr, m.H, m.final_norm};
-        build_frags(c, a, allH);
+        build_frags(a, allH);
         ssq_block(c, 2);
         bar_consumers();
-        cons_gemv(c, ST_LM, m.layers[0], &c.rt[0], ci);
+        cons_gemv(c, ST_LM, c.misc->L[0], &c.rt[0], ci);
         if (!grid_sync(c, 8)) return;
     }
     // ---- logits, per-CTA argmax candidates
@@ -1513,30 +1948,54 @@ __device__ void consumer(Ctx &c) {
         int *bi = reinterpret_cast<int *>(c.sm + SM_SCRATCH + 4096);
         int b, e;
         split_range(m.V, c.G, c.cta, b, e);
-        for (int t = 0; t < c.T; ++t) {
-            float inv = c.misc->inv_rms[2][t];
-            float best = -CUDART_INF_F;
-            int besti = 0x7fffffff;
-            for (int v = b + c.tid; v < e; v += MK_NCWARPS * 32) {
-                float lg = from_fx(__ldcg(m.logit_acc + (long long)t * m.V + v)) * inv;
-                p.out_logits[(long long)t * m.V + v] = lg;
-                if (lg > best || (lg == best && v < besti)) {
-                    best = lg;
-                    besti = v;
-                }
+        float best[MK_MAXT];
+        int besti[MK_MAXT];
+#pragma unroll
+        for (int t = 0; t < MK_MAXT; ++t) {
+            best[t] = -CUDART_INF_F;
+            besti[t] = 0x7fffffff;
+        }
+        for (int v0 = b + c.tid; v0 < e; v0 += 4 * MK_NCWARPS * 32) {
+            long long raw[4][MK_MAXT];
+#pragma unroll
+            for (int u4 = 0; u4 < 4; ++u4) {
+                int v = v0 + u4 * MK_NCWARPS * 32;
+#pragma unroll
+                for (int t = 0; t < MK_MAXT; ++t)
+                    raw[u4][t] = (v < e && t < c.T) ? __ldcg(m.logit_acc + (long long)t * m.V + v) : 0;
             }
 #pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                float ob = __shfl_xor_sync(0xffffffffu, best, o);
-                int oi = __shfl_xor_sync(0xffffffffu, besti, o);
-                if (ob > best || (ob == best && oi < besti)) {
-                    best = ob;
-                    besti = oi;
+            for (int u4 = 0; u4 < 4; ++u4) {
+                int v = v0 + u4 * MK_NCWARPS * 32;
+                if (v >= e) break;
+#pragma unroll
+                for (int t = 0; t < MK_MAXT; ++t) {
+                    if (t >= c.T) break;
+                    float lg = from_fx(raw[u4][t]) * c.misc->inv_rms[2][t];
+                    __stcs(p.out_logits + (long long)t * m.V + v, lg);
+                    if (lg > best[t] || (lg == best[t] && v < besti[t])) {
+                        best[t] = lg;
+                        besti[t] = v;
+                    }
                 }
             }
-            if (c.lane == 0) {
-                bv[t * 8 + c.warp] = best;
-                bi[t * 8 + c.warp] = besti;
+        }
+#pragma unroll
+        for (int t = 0; t < MK_MAXT; ++t) {
+            float bb = best[t];
+            int bi2 = besti[t];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                float ob = __shfl_xor_sync(0xffffffffu, bb, o);
+                int oi = __shfl_xor_sync(0xffffffffu, bi2, o);
+                if (ob > bb || (ob == bb && oi < bi2)) {
+                    bb = ob;
+                    bi2 = oi;
+                }
+            }
+            if (c.lane == 0 && t < c.T) {
+                bv[t * 8 + c.warp] = bb;
+                bi[t * 8 + c.warp] = bi2;
             }
         }
         bar_consumers();
@@ -1588,53 +2047,50 @@ __device__ void consumer(Ctx &c) {
             k->distinct_sum += c.misc->distinct_total;
             k->last_accepted = n;
             k->last_distinct = c.misc->distinct_total;
-            k->epoch = c.bar_base + (unsigned long long)c.nbar * c.G;
+            k->epoch = c.misc->base + (unsigned long long)c.misc->nbar * c.G;
         }
     }
 }
 
 __global__ void __launch_bounds__(MK_THREADS, 1) mk_step_kernel(const __grid_constant__ Params p) {
-    extern __shared__ unsigned char smem_raw[];
-    // the 128-byte TMA swizzle pattern repeats every 1024 bytes: align the map to it
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    Ctx c;
-    c.p = &p;
-    c.m = p.m;
-    c.ctrl = p.m->ctrl;
-    c.sm = smem;
-    c.full = reinterpret_cast<uint64_t *>(smem + SM_BAR);
-    c.empty = c.full + MK_RING;
-    c.route = c.empty + MK_RING;
-    c.rt = reinterpret_cast<RouteSm *>(smem + SM_ROUTE);
-    c.misc = reinterpret_cast<MiscSm *>(smem + SM_MISC);
-    c.cta = blockIdx.x;
-    c.G = gridDim.x;
-    c.T = p.T;
-    c.tid = threadIdx.x;
-    c.warp = threadIdx.x >> 5;
-    c.lane = threadIdx.x & 31;
-    c.nbar = 0;
-    c.timeout = p.m->timeout_ns;
-    const DModel &m = *p.m;
+    unsigned char *smem = smem_base();
+    MiscSm *misc = reinterpret_cast<MiscSm *>(smem + SM_MISC);
+    const DModel *gm = p.m;
+    // model block and first layer's descriptors into shared memory
+    {
+        const int nw = (int)(sizeof(DModel) / 4);
+        for (int i = threadIdx.x; i < nw; i += blockDim.x)
+            reinterpret_cast<uint32_t *>(&misc->m)[i] = __ldg(reinterpret_cast<const uint32_t *>(gm) + i);
+        const int nl = (int)(sizeof(DLayer) / 4);
+        const DLayer *l0 = gm->layers + (p.mode ? p.layer : 0);
+        for (int i = threadIdx.x; i < nl; i += blockDim.x)
+            reinterpret_cast<uint32_t *>(&misc->L[0])[i] = __ldg(reinterpret_cast<const uint32_t *>(l0) + i);
+    }
     if (threadIdx.x == 0) {
+        uint64_t *full = reinterpret_cast<uint64_t *>(smem + SM_BAR), *empty = full + MK_RING,
+                 *route = empty + MK_RING;
         for (int i = 0; i < MK_RING; ++i) {
-            mbar_init(&c.full[i], 1);
-            mbar_init(&c.empty[i], MK_NCWARPS);
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], MK_NCWARPS);
         }
-        mbar_init(c.route, 1);
+        mbar_init(route, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        c.misc->abort = 0;
-        c.misc->distinct_total = 0;
+        misc->abort = 0;
+        misc->distinct_total = 0;
+        misc->nbar = 0;
+        misc->nmark = 0;
+        misc->p = &p;
+        Ctrl *ctrl = gm->ctrl;
         // validate the step's inputs (every CTA reaches the same verdict)
+        const int P = gm->P;
         int ctx = __ldg(p.positions);
-        int ok = (*(volatile int *)&c.ctrl->abort == 0) ? 1 : 0;
+        int ok = (*(volatile int *)&ctrl->abort == 0) ? 1 : 0;
         for (int t = 0; t < p.T; ++t)
             if (__ldg(p.positions + t) != ctx + t) ok = 0;
-        if (ctx < 0 || (long long)ctx + p.T > (long long)m.max_pages * m.P) ok = 0;
+        if (ctx < 0 || (long long)ctx + p.T > (long long)gm->max_pages * P) ok = 0;
         if (ok) {
-            int np = (ctx + p.T + m.P - 1) / m.P;
+            int np = (ctx + p.T + P - 1) / P;
             for (int j = 0; j < np; ++j) {
                 int ph = __ldg(p.page_table + j);
                 if (ph < 0 || ph >= p.n_pages) ok = 0;
@@ -1643,32 +2099,30 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_step_kernel(const __grid_con
         if (ok && p.mode == 0) {
             for (int t = 0; t < p.T; ++t) {
                 int tk = __ldg(p.tokens + t);
-                if (tk < 0 || tk >= m.V) ok = 0;
+                if (tk < 0 || tk >= gm->V) ok = 0;
             }
         }
-        c.misc->valid = ok;
-        c.misc->ctx = ctx;
-        c.misc->base = *(volatile unsigned long long *)&c.ctrl->epoch;
+        misc->valid = ok;
+        misc->ctx = ok ? ctx : 0;
+        const int ncp = (misc->ctx + P - 1) / P;
+        misc->nsplit = min(min((int)gridDim.x / gm->Hkv, (ncp + 1 + MK_ATT_MIN_PAGES - 1) / MK_ATT_MIN_PAGES),
+                           MK_MAXSPLIT);
+        misc->base = *(volatile unsigned long long *)&ctrl->epoch;
     }
     __syncthreads();
-    if (!c.misc->valid) {
-        if (blockIdx.x == 0 && threadIdx.x == 0 && *(volatile int *)&c.ctrl->abort == 0) {
-            atomicCAS(&c.ctrl->status, 0, (int)MK_ERR_BAD_INPUT);
-            atomicExch(&c.ctrl->abort, 1);
+    if (!misc->valid) {
+        Ctrl *ctrl = gm->ctrl;
+        if (blockIdx.x == 0 && threadIdx.x == 0 && *(volatile int *)&ctrl->abort == 0) {
+            atomicCAS(&ctrl->status, 0, (int)MK_ERR_BAD_INPUT);
+            atomicExch(&ctrl->abort, 1);
         }
         return;
     }
-    c.ctx = c.misc->ctx;
-    c.bar_base = c.misc->base;
-    {
-        int ncp = (c.ctx + m.P - 1) / m.P;
-        c.nsplit = min(min(c.G / m.Hkv, ncp + 1), MK_MAXSPLIT);
-    }
-    if (c.warp == MK_NCWARPS) {
-        if (c.lane == 0) producer(c);
+    if ((threadIdx.x >> 5) == MK_NCWARPS) {
+        if ((threadIdx.x & 31) < MK_PLANES) producer();
         __syncwarp();
     } else {
-        consumer(c);
+        consumer();
     }
 }
 

@@ -22,7 +22,7 @@ MK_DESC_VERSION = 1
 
 #: every symbol include/mk.h declares
 EXPORTS = ["mk_create", "mk_decode_step", "mk_decode_step_host", "mk_layer_forward",
-           "mk_get_status", "mk_get_stats", "mk_set_routing_trace", "mk_reset", "mk_destroy", "mk_status_string",
+           "mk_get_status", "mk_get_stats", "mk_set_routing_trace", "mk_set_stage_trace", "mk_reset", "mk_destroy", "mk_status_string",
            "mk_last_error"]
 
 _vp = ctypes.c_void_p
@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
     L.mk_layer_forward.restype = S
     L.mk_set_routing_trace.argtypes = [_vp, _vp]
     L.mk_set_routing_trace.restype = S
+    L.mk_set_stage_trace.argtypes = [_vp, _vp, ctypes.c_int, _vp]
+    L.mk_set_stage_trace.restype = S
     L.mk_get_status.argtypes = [_vp]
     L.mk_get_status.restype = S
     L.mk_get_stats.argtypes = [_vp, ctypes.POINTER(mk_stats)]
@@ -169,6 +171,10 @@ def mk_layer_forward(st, layer, hidden_in, T, positions, kv: mk_kv_cache, hidden
 
 def mk_set_routing_trace(st, trace) -> int:
     return _check(st, lib().mk_set_routing_trace(st, _ptr(trace)))
+
+
+def mk_set_stage_trace(st, times, capacity=0, events=None) -> int:
+    return _check(st, lib().mk_set_stage_trace(st, _ptr(times), capacity, _ptr(events)))
 
 
 def mk_get_status(st) -> int:
