@@ -187,6 +187,40 @@ mk_status mk_layer_forward(mk_state *st, int layer, const float *hidden_in, int 
                            float *hidden_out, int32_t *out_topk_idx, float *out_topk_w,
                            void *stream);
 
+/* mk_layer_forward without a state and without any device allocation.
+ *
+ * For callers that cannot call cudaMalloc: a runtime without a device
+ * allocator, a host application that owns all device memory, or code that must
+ * not allocate once serving has started (allocation can block, fragment the
+ * pool or fail under memory pressure).  The pages have no counterpart: it is
+ * an integration entry point.
+ *
+ * Runs layer `layer`'s computation exactly as mk_layer_forward does (same
+ * kernel, same results) for a model described by desc (n_layers is ignored)
+ * with that layer's weights lw; the KV pools, page table and positions are the
+ * caller's as in mk_layer_forward, with ctx = positions[0] also passed on the
+ * host.  All other state -- the model block, TMA descriptors, RoPE rows,
+ * control block and accumulators -- lives in one file-scope device array of
+ * 24 MiB that every device which loads this library holds until the process
+ * exits.  A model whose working set does not fit returns MK_ERR_UNSUPPORTED
+ * (a layer of hidden 4096, 32/4 heads of 128, 384 experts of width 512 takes
+ * about 23 MiB).  out_status (dev int32 [1], may be NULL) receives the device
+ * status (MK_OK, MK_ERR_BAD_INPUT or MK_ERR_TIMEOUT) in stream order.
+ *
+ * The first call on a device does that device's set-up (finding the array's
+ * device address, the kernel's shared-memory attribute); make it with the
+ * device current and before any stream capture.  Every call reuses the same
+ * array, so calls that may overlap on the device (different streams without
+ * ordering, several host threads) race and give wrong results: serialise them.
+ * Each call clears the control block it needs; nothing else must start at zero.
+ * No call allocates device or host memory. */
+mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const mk_layer_weights *lw,
+                                   void *k_pool, void *v_pool, const int32_t *page_table,
+                                   int n_pages, const float *hidden_in, int T, int ctx,
+                                   const int32_t *positions, float *hidden_out,
+                                   int32_t *out_topk_idx, float *out_topk_w,
+                                   int32_t *out_status, void *stream);
+
 /* Record, on every later mk_decode_step, each layer's selected experts into
  * trace (dev int32 [n_layers][T][top_k], key order); NULL turns it off.  The
  * buffer must stay valid while tracing is on.  Used to check routing layer by

@@ -4,8 +4,10 @@
 
 #include <cmath>
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "mk_internal.h"
@@ -508,3 +510,246 @@ mk_status mk_reset(mk_state *st) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// mk_layer_forward_noalloc: the same kernel in one-layer mode, for callers that
+// cannot allocate device memory (an allocator-less runtime, a plugin host that
+// owns all device memory, code that must not allocate after start-up or while
+// a CUDA graph is being captured).  Everything the launch needs besides the
+// caller's tensors -- the model block, the layer's TMA descriptors, the RoPE
+// rows of the step, the control block and all accumulators -- is carved out of
+// one file-scope device array, so no call allocates.
+// ---------------------------------------------------------------------------
+#define MK_NOALLOC_SCRATCH_BYTES (24u << 20)  // 24 MiB, held by every device that loads the library
+static __device__ __align__(256) unsigned char g_mk_noalloc_scratch[MK_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+struct NoallocDevice {
+    bool ready;
+    unsigned char *scratch;   // device address of g_mk_noalloc_scratch on this device
+    int grid;
+    size_t smem;
+    PFN_cuTensorMapEncodeTiled_v12000 encode;
+};
+constexpr int kMaxDevices = 64;
+NoallocDevice g_noalloc[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// per-device set-up, run by the first call on a device with that device current
+mk_status noalloc_setup(mk_state *st, int dev, NoallocDevice **out) {
+    if (dev < 0 || dev >= kMaxDevices) return fail(st, MK_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoallocDevice &d = g_noalloc[dev];
+    if (!d.ready) {
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_mk_noalloc_scratch);
+        if (e != cudaSuccess || !ptr) return fail(st, MK_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return fail(st, MK_ERR_CUDA, "cudaGetDeviceProperties");
+        if (prop.major != 10 || prop.minor != 3)
+            return fail(st, MK_ERR_UNSUPPORTED, "built for compute capability 10.3, device is %d.%d", prop.major, prop.minor);
+        const size_t smem = SM_TOTAL + 1024;
+        if (mk_kernel_setup(smem) != cudaSuccess) return fail(st, MK_ERR_CUDA, "cudaFuncSetAttribute");
+        if (mk_kernel_max_blocks(smem) < 1) return fail(st, MK_ERR_UNSUPPORTED, "persistent CTA does not fit on an SM");
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return fail(st, MK_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled not available");
+        d.scratch = static_cast<unsigned char *>(ptr);
+        d.grid = prop.multiProcessorCount;
+        d.smem = smem;
+        d.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        d.ready = true;
+    }
+    *out = &d;
+    return MK_OK;
+}
+
+// bump allocator over the static array (offsets only; nothing is allocated)
+struct Carve {
+    size_t off = 0;
+    template <class T>
+    size_t take(size_t bytes) {
+        size_t o = (off + 255) & ~(size_t)255;
+        off = o + (bytes ? bytes : 16);
+        return o;
+    }
+};
+}  // namespace
+
+extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const mk_layer_weights *lw,
+                                              void *k_pool, void *v_pool, const int32_t *page_table,
+                                              int n_pages, const float *hidden_in, int T, int ctx,
+                                              const int32_t *positions, float *hidden_out,
+                                              int32_t *out_topk_idx, float *out_topk_w,
+                                              int32_t *out_status, void *stream) {
+    mk_state local;  // carries the error text and the encode entry point; owns nothing
+    mk_state *st = &local;
+    auto ret = [&](mk_status s) {
+        snprintf(g_create_err, sizeof(g_create_err), "%s", st->err);
+        return s;
+    };
+#define CKN(call)                                                                                  \
+    do {                                                                                           \
+        cudaError_t e_ = (call);                                                                   \
+        if (e_ != cudaSuccess) return ret(fail(st, MK_ERR_CUDA, "%s: %s", #call, cudaGetErrorString(e_))); \
+    } while (0)
+    if (!desc || !lw || !k_pool || !v_pool || !page_table || !hidden_in || !hidden_out || !positions)
+        return ret(fail(st, MK_ERR_INVALID, "null pointer argument"));
+    mk_status r = check_desc(st, desc);
+    if (r != MK_OK) return ret(r);
+    mk_model_desc d = *desc;
+    if (T < 1 || T > d.max_T) return ret(fail(st, MK_ERR_INVALID, "T = %d outside [1, %d]", T, d.max_T));
+    if (ctx < 0 || (long long)ctx + T > (long long)d.max_pages_per_stream * d.page_size)
+        return ret(fail(st, MK_ERR_INVALID, "ctx %d + T exceeds the page table", ctx));
+    if (n_pages < 1) return ret(fail(st, MK_ERR_INVALID, "n_pages < 1"));
+    if (hidden_in == hidden_out) return ret(fail(st, MK_ERR_INVALID, "hidden_in and hidden_out alias"));
+    if (d.timeout_ms <= 0) d.timeout_ms = 1000;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ret(fail(st, MK_ERR_CUDA, "no CUDA device"));
+    NoallocDevice *nd = nullptr;
+    if ((r = noalloc_setup(st, dev, &nd)) != MK_OK) return ret(r);
+    st->encode = nd->encode;
+
+    const int H = d.hidden, Hq = d.n_q_heads, Hkv = d.n_kv_heads, hd = d.head_dim;
+    const int E = d.n_experts, I = d.expert_inter, nqkv = (Hq + 2 * Hkv) * hd;
+    const size_t T8 = MK_MAXT;
+    // layout of the static array for this model
+    Carve cv;
+    const size_t o_model = cv.take<DModel>(sizeof(DModel));
+    const size_t o_layer = cv.take<DLayer>(sizeof(DLayer));
+    const size_t o_maps = cv.take<CUtensorMap>(11 * sizeof(CUtensorMap));
+    const size_t o_pools = cv.take<void *>(2 * sizeof(void *));
+    const size_t o_rope = cv.take<float2>(T8 * (hd / 2) * sizeof(float2));
+    const size_t o_ctrl = cv.take<Ctrl>(sizeof(Ctrl));
+    const size_t o_attcnt = cv.take<int>(sizeof(int) * Hkv);
+    const size_t o_qkv = cv.take<long long>(8 * T8 * nqkv);
+    const size_t o_res = cv.take<long long>(8 * T8 * H);
+    const size_t o_rlog = cv.take<long long>(8 * T8 * E);
+    const size_t o_sh = cv.take<long long>(8 * T8 * 2 * I);
+    const size_t o_ea = cv.take<long long>(8 * T8 * d.top_k * 2 * I);
+    const size_t o_logit = cv.take<long long>(8 * T8);
+    const size_t o_ssq = cv.take<float>(4 * 3 * MK_MAXKB * T8);
+    const size_t o_obuf = cv.take<float>(4 * T8 * Hq * hd);
+    const size_t o_part = cv.take<float>(4ull * Hkv * MK_MAXSPLIT * MK_MAXROWS * (hd + 2));
+    const size_t o_candv = cv.take<float>(4 * T8 * nd->grid);
+    const size_t o_candi = cv.take<int>(4 * T8 * nd->grid);
+    if (cv.off > MK_NOALLOC_SCRATCH_BYTES)
+        return ret(fail(st, MK_ERR_UNSUPPORTED, "model needs %zu bytes of scratch; mk_layer_forward_noalloc has %u",
+                        cv.off, (unsigned)MK_NOALLOC_SCRATCH_BYTES));
+    unsigned char *base = nd->scratch;
+
+    // descriptors of the layer's matrices and of its KV pools
+    CUtensorMap maps[11];
+    DLayer dl;
+    memset(&dl, 0, sizeof(dl));
+    dl.attn_norm = lw->attn_norm;
+    dl.moe_norm = lw->moe_norm;
+    dl.router_bias = lw->router_bias;
+    if (!lw->attn_norm || !lw->moe_norm || !lw->router_bias) return ret(fail(st, MK_ERR_INVALID, "null norm or bias"));
+    if (d.n_shared && (!lw->ws1 || !lw->ws3 || !lw->ws2)) return ret(fail(st, MK_ERR_INVALID, "n_shared = 1 needs ws1/ws3/ws2"));
+    const int wd = d.weight_dtype;
+    MatSpec specs[9] = {
+        {lw->w_qkv, lw->w_qkv_scale, wd, nqkv, H, 1},   {lw->w_o, lw->w_o_scale, wd, H, Hq * hd, 1},
+        {lw->w_router, nullptr, d.router_dtype, E, H, 1}, {lw->w1, lw->w1_scale, wd, I, H, E},
+        {lw->w3, lw->w3_scale, wd, I, H, E},             {lw->w2, lw->w2_scale, wd, H, I, E},
+        {d.n_shared ? lw->ws1 : nullptr, lw->ws1_scale, wd, I, H, 1},
+        {d.n_shared ? lw->ws3 : nullptr, lw->ws3_scale, wd, I, H, 1},
+        {d.n_shared ? lw->ws2 : nullptr, lw->ws2_scale, wd, H, I, 1},
+    };
+    DMat *dm[9] = {&dl.qkv, &dl.o, &dl.router, &dl.w1, &dl.w3, &dl.w2, &dl.s1, &dl.s3, &dl.s2};
+    int nmaps = 0;
+    for (int k = 0; k < 9; ++k) {
+        if (k < 6 && !specs[k].w) return ret(fail(st, MK_ERR_INVALID, "null weight %d", k));
+        DMat &m = *dm[k];
+        memset(&m, 0, sizeof(m));
+        if (!specs[k].w) continue;
+        const MatSpec &sp = specs[k];
+        m.dtype = sp.dtype;
+        m.rows = sp.rows;
+        m.cols = sp.cols;
+        m.es = dt_size(sp.dtype);
+        m.n_rg = (sp.rows + 255) / 256;
+        m.n_kc = sp.cols * m.es / 128;
+        m.is3d = sp.E > 1;
+        m.scale = sp.scale;
+        m.scale_estride = (long long)(sp.cols / 128) * sp.rows;
+        if (sp.dtype == MK_DT_FP8E4M3_B128 && (!sp.scale || reinterpret_cast<uintptr_t>(sp.scale) % 16))
+            return ret(fail(st, MK_ERR_INVALID, "FP8 matrix needs 16-byte aligned scales"));
+        if ((r = encode_map(st, &maps[nmaps], sp.w, m.es, sp.cols, sp.rows, sp.E, 256)) != MK_OK) return ret(r);
+        m.tmap = reinterpret_cast<const CUtensorMap *>(base + o_maps) + nmaps;
+        ++nmaps;
+    }
+    const int kv_es = dt_size(d.kv_dtype);
+    const long long kv_rows = (long long)n_pages * Hkv * d.page_size;
+    if ((r = encode_map(st, &maps[9], k_pool, kv_es, hd, kv_rows, 1, d.page_size)) != MK_OK) return ret(r);
+    if ((r = encode_map(st, &maps[10], v_pool, kv_es, hd, kv_rows, 1, d.page_size)) != MK_OK) return ret(r);
+
+    // RoPE rows of positions ctx..ctx+T-1 (fp64 angles, stored fp32); the model
+    // block points the table so that the kernel's absolute index lands on them
+    float2 rope[MK_MAXT * 64];
+    for (int t = 0; t < T; ++t)
+        for (int i = 0; i < hd / 2; ++i) {
+            double a = (double)(ctx + t) * std::pow((double)d.rope_base, -2.0 * i / hd);
+            rope[t * (hd / 2) + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+        }
+
+    DModel hm;
+    memset(&hm, 0, sizeof(hm));
+    hm.L = 1; hm.H = H; hm.Hq = Hq; hm.Hkv = Hkv; hm.d = hd; hm.E = E; hm.K = d.top_k; hm.I = I;
+    hm.V = 0; hm.P = d.page_size; hm.nshared = d.n_shared; hm.max_pages = d.max_pages_per_stream;
+    hm.maxT = d.max_T; hm.G = nd->grid; hm.wdt = d.weight_dtype; hm.rdt = d.router_dtype;
+    hm.kvdt = d.kv_dtype; hm.kv_es = kv_es; hm.nqkv = nqkv; hm.eps = d.rms_eps;
+    hm.timeout_ns = (long long)d.timeout_ms * 1000000ll;
+    hm.layers = reinterpret_cast<const DLayer *>(base + o_layer);
+    hm.rope = reinterpret_cast<const float2 *>(base + o_rope) - (long long)ctx * (hd / 2);
+    hm.ctrl = reinterpret_cast<Ctrl *>(base + o_ctrl);
+    hm.att_cnt = reinterpret_cast<int *>(base + o_attcnt);
+    hm.qkv_acc = reinterpret_cast<long long *>(base + o_qkv);
+    hm.res = reinterpret_cast<long long *>(base + o_res);
+    hm.rlog = reinterpret_cast<long long *>(base + o_rlog);
+    hm.sh_acc = reinterpret_cast<long long *>(base + o_sh);
+    hm.ea_acc = reinterpret_cast<long long *>(base + o_ea);
+    hm.logit_acc = reinterpret_cast<long long *>(base + o_logit);
+    hm.ssq = reinterpret_cast<float *>(base + o_ssq);
+    hm.o_buf = reinterpret_cast<float *>(base + o_obuf);
+    hm.att_part = reinterpret_cast<float *>(base + o_part);
+    hm.cand_v = reinterpret_cast<float *>(base + o_candv);
+    hm.cand_i = reinterpret_cast<int *>(base + o_candi);
+    void *pools[2] = {k_pool, v_pool};
+
+    // stage the launch's tables into the array (stream-ordered copies; the host
+    // buffers may be reused once the calls return) and clear the control block
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    CKN(cudaMemcpyAsync(base + o_model, &hm, sizeof(hm), cudaMemcpyHostToDevice, s));
+    CKN(cudaMemcpyAsync(base + o_layer, &dl, sizeof(dl), cudaMemcpyHostToDevice, s));
+    CKN(cudaMemcpyAsync(base + o_maps, maps, sizeof(maps), cudaMemcpyHostToDevice, s));
+    CKN(cudaMemcpyAsync(base + o_pools, pools, sizeof(pools), cudaMemcpyHostToDevice, s));
+    CKN(cudaMemcpyAsync(base + o_rope, rope, sizeof(float2) * T * (hd / 2), cudaMemcpyHostToDevice, s));
+    CKN(cudaMemsetAsync(base + o_ctrl, 0, sizeof(Ctrl), s));
+
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.m = reinterpret_cast<const DModel *>(base + o_model);
+    p.kvmaps = reinterpret_cast<const CUtensorMap *>(base + o_maps) + 9;
+    p.kpool = reinterpret_cast<void *const *>(base + o_pools);
+    p.vpool = reinterpret_cast<void *const *>(base + o_pools) + 1;
+    p.page_table = page_table;
+    p.positions = positions;
+    p.T = T;
+    p.mode = 1;
+    p.layer = 0;
+    p.n_pages = n_pages;
+    p.hidden_in = hidden_in;
+    p.hidden_out = hidden_out;
+    p.out_idx = out_topk_idx;
+    p.out_w = out_topk_w;
+    cudaError_t e = mk_launch(p, nd->grid, nd->smem, s);
+    if (e != cudaSuccess) return ret(fail(st, MK_ERR_CUDA, "launch: %s", cudaGetErrorString(e)));
+    if (out_status)
+        CKN(cudaMemcpyAsync(out_status, base + o_ctrl + offsetof(Ctrl, status), sizeof(int32_t),
+                           cudaMemcpyDeviceToDevice, s));
+    return MK_OK;
+#undef CKN
+}

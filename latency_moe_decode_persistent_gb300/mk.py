@@ -22,7 +22,7 @@ MK_DESC_VERSION = 1
 
 #: every symbol include/mk.h declares
 EXPORTS = ["mk_create", "mk_decode_step", "mk_decode_step_host", "mk_layer_forward",
-           "mk_get_status", "mk_get_stats", "mk_set_routing_trace", "mk_set_stage_trace", "mk_reset", "mk_destroy", "mk_status_string",
+           "mk_get_status", "mk_get_stats", "mk_set_routing_trace", "mk_set_stage_trace", "mk_reset", "mk_layer_forward_noalloc", "mk_destroy", "mk_status_string",
            "mk_last_error"]
 
 _vp = ctypes.c_void_p
@@ -90,6 +90,11 @@ def lib() -> ctypes.CDLL:
     L.mk_layer_forward.argtypes = [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp,
                                    ctypes.POINTER(mk_kv_cache), _vp, _vp, _vp, _vp]
     L.mk_layer_forward.restype = S
+    L.mk_layer_forward_noalloc.argtypes = [ctypes.POINTER(mk_model_desc),
+                                           ctypes.POINTER(mk_layer_weights), _vp, _vp, _vp,
+                                           ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
+                                           _vp, _vp, _vp, _vp]
+    L.mk_layer_forward_noalloc.restype = S
     L.mk_set_routing_trace.argtypes = [_vp, _vp]
     L.mk_set_routing_trace.restype = S
     L.mk_set_stage_trace.argtypes = [_vp, _vp, ctypes.c_int, _vp]
@@ -167,6 +172,16 @@ def mk_layer_forward(st, layer, hidden_in, T, positions, kv: mk_kv_cache, hidden
                                _ptr(hidden_out), _ptr(out_topk_idx), _ptr(out_topk_w),
                                _ptr(stream))
     return _check(st, s) if check else s
+
+
+def mk_layer_forward_noalloc(desc: mk_model_desc, lw: mk_layer_weights, k_pool, v_pool, page_table,
+                             n_pages, hidden_in, T, ctx, positions, hidden_out, out_topk_idx=None,
+                             out_topk_w=None, out_status=None, stream=None, check=True) -> int:
+    s = lib().mk_layer_forward_noalloc(ctypes.byref(desc), ctypes.byref(lw), _ptr(k_pool),
+                                       _ptr(v_pool), _ptr(page_table), n_pages, _ptr(hidden_in), T,
+                                       ctx, _ptr(positions), _ptr(hidden_out), _ptr(out_topk_idx),
+                                       _ptr(out_topk_w), _ptr(out_status), _ptr(stream))
+    return _check(None, s) if check else s
 
 
 def mk_set_routing_trace(st, trace) -> int:
