@@ -82,6 +82,38 @@ __device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int x, 
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(sa(bar))
         : "memory");
 }
+// the same copies with an L2 eviction-priority hint (streamed weights are read
+// once per step: evict them first so that activations, accumulators, tensor
+// maps and code stay resident in L2)
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void tma2d_h(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                        uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(sa(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(sa(bar)), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma3d_h(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                        uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(sa(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(sa(bar)), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_h(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                           uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(sa(dst)),
+        "l"(src), "r"(bytes), "r"(sa(bar)), "l"(pol)
+        : "memory");
+}
 __device__ __forceinline__ void tma_prefetch2d(const CUtensorMap *map, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
                  : "memory");
@@ -169,9 +201,30 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
 }
-__device__ __forceinline__ long long to_fx(float v) { return __float2ll_rn(v * MK_FX); }
+// Fixed-point (2^-32) conversions.  The 64-bit integer <-> float conversion
+// instructions issue on the FP64 pipe, which on this part runs at a small
+// fraction of the integer and FP32 rate, so both directions are built from
+// 32-bit operations.
+// to_fx: |v| * 2^32 rounded half away from zero, from the float's fields
+// (|v| < 2^31; zero and subnormal inputs give 0).
+__device__ __forceinline__ long long to_fx(float v) {
+    const uint32_t b = __float_as_uint(v);
+    const int e = (int)((b >> 23) & 0xffu);
+    const uint32_t m = (b & 0x7fffffu) | 0x800000u;
+    const int s = e - 118;  // |v| * 2^32 = m * 2^(e - 118)
+    unsigned long long r;
+    if (s >= 0) r = (unsigned long long)m << min(s, 39);
+    else if (s > -25) r = (m + (1u << (-s - 1))) >> (-s);
+    else r = 0;
+    if (e == 0) r = 0;
+    return (b >> 31) ? -(long long)r : (long long)r;
+}
+// from_fx: magnitude split into 32-bit halves, each converted exactly or
+// rounded once, then recombined (at most one extra rounding of the sum).
 __device__ __forceinline__ float from_fx(long long v) {
-    return __ll2float_rn(v) * (1.0f / MK_FX);
+    const unsigned long long a = v < 0 ? 0ull - (unsigned long long)v : (unsigned long long)v;
+    const float f = fmaf(__uint2float_rn((uint32_t)a), 1.0f / MK_FX, __uint2float_rn((uint32_t)(a >> 32)));
+    return v < 0 ? -f : f;
 }
 __device__ __forceinline__ void red_add(long long *p, long long v) {
     atomicAdd(reinterpret_cast<unsigned long long *>(p), (unsigned long long)v);
@@ -572,6 +625,7 @@ __device__ void stage_iter(StageIter &it, const Ctx &c, int st, const DLayer &L,
 
 // producer-side state of one issuing lane (registers of the producer)
 struct Prod {
+    uint64_t pol;                 // L2 evict-first policy of streamed weights and KV pages
     uint32_t pi;                  // ring positions handed out so far
     int last;                     // last position this lane armed (-1: none)
     unsigned long long wait, tma, bulk;
@@ -621,12 +675,12 @@ __device__ __forceinline__ bool prod_gemv_impl(const Ctx &c, Prod &ps, int st, c
         void *dst = ring + slot * MK_SLOT;
         const int x = it.kc * d.xstep, y = it.rg * 256;
         unsigned long long t0 = c.prof ? clock64() : 0;
-        if (d.is3d) tma3d(dst, d.tmap, x, y, e, &full[slot]);
-        else tma2d(dst, d.tmap, x, y, &full[slot]);
+        if (d.is3d) tma3d_h(dst, d.tmap, x, y, e, &full[slot], ps.pol);
+        else tma2d_h(dst, d.tmap, x, y, &full[slot], ps.pol);
         unsigned long long t1 = c.prof ? clock64() : 0;
         if (sbytes) {
             const float *src = d.scale + (long long)e * d.sest + (long long)it.kc * d.rows + y;
-            bulk_g2s(sbase + slot * 1024, src, sbytes, &full[slot]);
+            bulk_g2s_h(sbase + slot * 1024, src, sbytes, &full[slot], ps.pol);
         }
         if (c.prof) {
             unsigned long long t2 = clock64();
@@ -642,7 +696,7 @@ __device__ __forceinline__ bool prod_gemv_impl(const Ctx &c, Prod &ps, int st, c
     return __all_sync((1u << MK_PLANES) - 1, ok);
 }
 
-__device__ __forceinline__ bool prod_gemv(const Ctx &c, Prod &ps, int st, const DLayer &L, const RouteSm *rt) {
+__device__ __noinline__ bool prod_gemv(const Ctx &c, Prod &ps, int st, const DLayer &L, const RouteSm *rt) {
     const bool prof = c.prof && c.lane == 0;
     unsigned long long cy0 = prof ? clock64() : 0, w0 = ps.wait, a0 = ps.tma, b0 = ps.bulk;
     bool ok = prod_gemv_impl(c, ps, st, L, rt);
@@ -674,8 +728,8 @@ __device__ __forceinline__ bool prod_att(const Ctx &c, Prod &ps, int l) {
         unsigned char *dst = c.sm + SM_RING + (pos % MK_RING) * MK_SLOT;
         uint64_t *bar = &c.full[pos % MK_RING];
         for (int bx = 0; bx < nbox; ++bx) {
-            tma2d(dst + bx * m.P * 128, km, bx * (128 / m.kv_es), y, bar);
-            tma2d(dst + MK_SLOT / 2 + bx * m.P * 128, vm, bx * (128 / m.kv_es), y, bar);
+            tma2d_h(dst + bx * m.P * 128, km, bx * (128 / m.kv_es), y, bar, ps.pol);
+            tma2d_h(dst + MK_SLOT / 2 + bx * m.P * 128, vm, bx * (128 / m.kv_es), y, bar, ps.pol);
         }
     }
     ps.pi += u.pc1 - u.p0;
@@ -688,6 +742,7 @@ __device__ __noinline__ void producer() {
     const DModel &m = *c.m;
     const Params &p = *c.p;
     Prod ps;
+    ps.pol = l2_evict_first();
     ps.pi = 0;
     ps.last = -1;
     ps.wait = ps.tma = ps.bulk = 0;
@@ -1051,7 +1106,9 @@ __device__ __forceinline__ void flush_item(const Ctx &c, int st, int ex, int mat
 }
 
 // consume this CTA's tiles of one GEMV stage
-__device__ __forceinline__ void cons_gemv(const Ctx &c, int st, const DLayer &L, const RouteSm *rt, uint32_t &ci) {
+__device__ __noinline__ uint32_t cons_gemv(int st, const DLayer *Lp, const RouteSm *rt, uint32_t ci) {
+    const Ctx c = make_ctx();
+    const DLayer &L = *Lp;
     StageIter it;
     stage_iter(it, c, st, L, rt);
     uint64_t *const full = c.full, *const empty = c.empty;
@@ -1108,6 +1165,7 @@ __device__ __forceinline__ void cons_gemv(const Ctx &c, int st, const DLayer &L,
         mark_val(c, MK_MARKS - 64 + st * 4 + 2, 900 + st * 4 + 2, cy_other);
     }
     mark(c, st * 16 + 2);
+    return ci;
 }
 
 // ------------------------------------------------------------------ small helpers
@@ -1862,7 +1920,7 @@ __device__ __noinline__ void consumer() {
             zero_slice(c, m.ea_acc, (long long)MK_MAXT * m.K * 2 * m.I);
             bar_consumers();
             mark(c, ST_QKV * 16 + 0);
-            cons_gemv(c, ST_QKV, L, rt, ci);
+            ci = cons_gemv(ST_QKV, &(L), rt, ci);
             if (!grid_sync(c, 2)) return;
         }
         // ---- attention
@@ -1882,7 +1940,7 @@ __device__ __noinline__ void consumer() {
             zero_slice(c, m.qkv_acc, (long long)MK_MAXT * m.nqkv);
             bar_consumers();
             mark(c, ST_O * 16 + 0);
-            cons_gemv(c, ST_O, L, rt, ci);
+            ci = cons_gemv(ST_O, &(L), rt, ci);
             if (!grid_sync(c, 4)) return;
         }
         // ---- router + shared expert gate/up, then routed gate/up
@@ -1893,9 +1951,9 @@ __device__ __noinline__ void consumer() {
             ssq_block(c, 1);
             bar_consumers();
             mark(c, ST_ROUTER * 16 + 0);
-            cons_gemv(c, ST_ROUTER, L, rt, ci);
+            ci = cons_gemv(ST_ROUTER, &(L), rt, ci);
             grid_arrive(c);
-            cons_gemv(c, ST_SHA, L, rt, ci);
+            ci = cons_gemv(ST_SHA, &(L), rt, ci);
             if (!grid_wait(c, 5)) return;
             compute_inv_rms(c, 1);
             bar_consumers();
@@ -1915,13 +1973,13 @@ __device__ __noinline__ void consumer() {
                         p.trace[(long long)l * c.T * m.K + i] = rt->idx[i / m.K][i % m.K];
                 }
             }
-            cons_gemv(c, ST_EXPA, L, rt, ci);
+            ci = cons_gemv(ST_EXPA, &(L), rt, ci);
             if (!grid_sync(c, 6)) return;
         }
         // ---- routed + shared down projections (+ residual)
         zero_slice(c, m.rlog, (long long)MK_MAXT * m.E);
         mark(c, ST_EXPB * 16 + 0);
-        cons_gemv(c, ST_EXPB, L, rt, ci);
+        ci = cons_gemv(ST_EXPB, &(L), rt, ci);
         if (!grid_sync(c, 7)) return;
     }
     if (p.mode == 1) {
@@ -1937,7 +1995,7 @@ __device__ __noinline__ void consumer() {
         build_frags(a, allH);
         ssq_block(c, 2);
         bar_consumers();
-        cons_gemv(c, ST_LM, c.misc->L[0], &c.rt[0], ci);
+        ci = cons_gemv(ST_LM, &(c.misc->L[0]), &c.rt[0], ci);
         if (!grid_sync(c, 8)) return;
     }
     // ---- logits, per-CTA argmax candidates
