@@ -58,14 +58,16 @@ struct DLayer {
     DMat qkv, o, router, w1, w3, w2, s1, s3, s2;
 };
 
-// control block in device memory
+// control block in device memory.  The barrier counter, which every CTA polls
+// at each grid barrier, has a cache line of its own so that the polling does
+// not contend with the status words.
 struct Ctrl {
-    unsigned long long bar_count;      // monotonic grid-barrier arrivals
-    unsigned long long epoch;          // bar_count at the start of the next launch
-    int abort;                         // set by the first failing wait
+    alignas(128) unsigned long long bar_count;  // monotonic grid-barrier arrivals
+    alignas(128) int abort;            // set by the first failing wait
     int status;                        // first device error (mk_status)
     int where;                         // diagnostic code of the failing wait
     int pad0;
+    unsigned long long epoch;          // bar_count at the start of the next launch
     unsigned long long steps, accepted_sum, distinct_sum;
     int last_accepted, last_distinct;
 };

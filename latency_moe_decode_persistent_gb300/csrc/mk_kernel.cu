@@ -332,8 +332,15 @@ __device__ __forceinline__ void mark_val(const Ctx &c, int slot, int id, unsigne
     }
 }
 
+// abort flag of this CTA (shared memory).  Only the grid-barrier thread reads
+// the device-wide flag and mirrors it here, so waiting threads never poll
+// global memory for it.
 __device__ __forceinline__ bool aborted(const Ctx &c) {
-    return *(volatile int *)&c.misc->abort != 0 || *(volatile int *)&c.ctrl->abort != 0;
+    return *(volatile int *)&c.misc->abort != 0;
+}
+__device__ __forceinline__ bool aborted_global(const Ctx &c) {
+    if (*(volatile int *)&c.ctrl->abort != 0) *(volatile int *)&c.misc->abort = 1;
+    return aborted(c);
 }
 __device__ void raise_err(const Ctx &c, int code, int where) {
     *(volatile int *)&c.misc->abort = 1;
@@ -362,6 +369,9 @@ __device__ void mbar_wait_drain(uint64_t *b, uint32_t parity, const Ctx &c) {
         if ((long long)(gtimer() - t0) > c.timeout) return;
     }
 }
+// spins of one thread on a counter in global memory: polls are spaced by a
+// short sleep after the first few so that many CTAs polling one line leave
+// the L2 slice that holds it free for other traffic
 __device__ bool spin_ge_u64(unsigned long long *a, unsigned long long target, const Ctx &c,
                             int where) {
     uint64_t t0 = 0;
@@ -369,8 +379,9 @@ __device__ bool spin_ge_u64(unsigned long long *a, unsigned long long target, co
         unsigned long long v;
         asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
         if (v >= target) return true;
-        if ((it & 31) == 31) {
-            if (aborted(c)) return false;
+        if (it >= 4) __nanosleep(64);
+        if ((it & 15) == 15) {
+            if (aborted_global(c)) return false;
             uint64_t now = gtimer();
             if (t0 == 0) t0 = now;
             else if ((long long)(now - t0) > c.timeout) {
@@ -386,8 +397,9 @@ __device__ bool spin_ge_s32(int *a, int target, const Ctx &c, int where) {
         int v;
         asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
         if (v >= target) return true;
-        if ((it & 31) == 31) {
-            if (aborted(c)) return false;
+        if (it >= 4) __nanosleep(64);
+        if ((it & 15) == 15) {
+            if (aborted_global(c)) return false;
             uint64_t now = gtimer();
             if (t0 == 0) t0 = now;
             else if ((long long)(now - t0) > c.timeout) {
@@ -413,7 +425,7 @@ __device__ void grid_arrive(const Ctx &c) {
 __device__ bool grid_wait(const Ctx &c, int where) {
     if (c.tid == 0) {
         const int nbar = c.misc->nbar;
-        bool ok = !aborted(c);
+        bool ok = !aborted_global(c);
         if (ok) ok = spin_ge_u64(&c.ctrl->bar_count, c.misc->base + (unsigned long long)nbar * c.G, c, where);
         __threadfence();
         c.misc->gs_ok = ok && !aborted(c);
@@ -803,45 +815,66 @@ __device__ __forceinline__ float4 act4(const ActSrc &a, int t, int col) {
     return v;
 }
 
-// build f16 fragments for the 128-column blocks in `mask` (consumer threads);
-// loads of eight blocks are issued before any is converted
+// byte offset, in the fragment buffer, of columns 4*c4 .. 4*c4+3 (c4 < 32) of
+// 128-column block kb for token t (the inverse of frag_col)
+__device__ __forceinline__ uint32_t frag_off(int kb, int t, int c4) {
+    const int q = c4 >> 3, sb = c4 & 1, x = (c4 >> 1) & 3;
+    return kb * 2048 + ((((x - 2 * (q >> 1)) & 3) * 32 + 4 * t + q) << 4) + sb * 8;
+}
+// zero the fragment columns of tokens T..7 in the blocks of `mask` (the MMA
+// always reduces against all eight token columns)
+__device__ __forceinline__ void frag_zero_pad(const Ctx &c, uint32_t mask) {
+    const int np = MK_MAXT - c.T;
+    if (np <= 0) return;
+    unsigned char *fr = c.sm + SM_SCRATCH;
+    const int n = __popc(mask) * np * 32;
+    for (int i = c.tid; i < n; i += MK_NCWARPS * 32) {
+        const int c4 = i & 31, r = i >> 5, k = r / np, t = c.T + (r - k * np);
+        *reinterpret_cast<uint2 *>(fr + frag_off(__fns(mask, 0, k + 1), t, c4)) = make_uint2(0, 0);
+    }
+}
+// build f16 fragments for the 128-column blocks in `mask` (consumer threads).
+// Work items are (block, token, 4-column group) with the column group fastest,
+// so each warp reads whole contiguous rows of the source (full L2 lines) and
+// scatters the converted values into fragment order in shared memory; eight
+// items per thread are in flight before any is converted.
 __device__ __noinline__ void build_frags(const ActSrc a, uint32_t mask) {
     const Ctx c = make_ctx();
-    const int s = c.tid >> 5, l = c.lane, n = l >> 2, q = l & 3;
-    const int col0 = frag_col(s, q, 0);
-    unsigned char *fr = c.sm + SM_SCRATCH + ((s >> 1) * 32 + l) * 16 + (s & 1) * 8;
-    const bool live = n < c.T;
-    const long long *fx = a.fx ? a.fx + (long long)n * a.stride + col0 : nullptr;
-    const float *f32 = a.f32 ? a.f32 + (long long)n * a.stride + col0 : nullptr;
-    for (int base = 0; base < MK_MAXKB; base += 4) {
-        const uint32_t mb = (mask >> base) & 0xfu;
-        if (!mb) continue;
-        longlong2 r0[4], r1[4];
-        float4 rf[4], g[4];
-        // phase 1: every load of the batch in flight
+    unsigned char *fr = c.sm + SM_SCRATCH;
+    frag_zero_pad(c, mask);
+    const int T = c.T, n = __popc(mask) * T * 32;
+    constexpr int B = 8, NT = MK_NCWARPS * 32;
+    for (int i0 = c.tid; i0 < n; i0 += B * NT) {
+        longlong2 x0[B], x1[B];
+        float4 xf[B], g[B];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int col = (base + i) * 128;
-            r0[i] = r1[i] = make_longlong2(0, 0);
-            rf[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            g[i] = make_float4(1.f, 1.f, 1.f, 1.f);
-            if (((mb >> i) & 1) && live) {
-                if (fx) {
-                    r0[i] = __ldcg(reinterpret_cast<const longlong2 *>(fx + col));
-                    r1[i] = __ldcg(reinterpret_cast<const longlong2 *>(fx + col) + 1);
+        for (int u = 0; u < B; ++u) {
+            const int i = i0 + u * NT;
+            x0[u] = x1[u] = make_longlong2(0, 0);
+            xf[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            g[u] = make_float4(1.f, 1.f, 1.f, 1.f);
+            if (i < n) {
+                const int c4 = i & 31, r = i >> 5, k = r / T, t = r - k * T;
+                const int col = __fns(mask, 0, k + 1) * 128 + 4 * c4;
+                if (a.fx) {
+                    const longlong2 *pp = reinterpret_cast<const longlong2 *>(a.fx + (long long)t * a.stride + col);
+                    x0[u] = __ldcg(pp);
+                    x1[u] = __ldcg(pp + 1);
                 } else {
-                    rf[i] = __ldcg(reinterpret_cast<const float4 *>(f32 + col));
+                    xf[u] = __ldcg(reinterpret_cast<const float4 *>(a.f32 + (long long)t * a.stride + col));
                 }
-                if (a.gamma) g[i] = __ldg(reinterpret_cast<const float4 *>(a.gamma + col0 + col));
+                if (a.gamma) g[u] = __ldg(reinterpret_cast<const float4 *>(a.gamma + col));
             }
         }
-        // phase 2: convert and store
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (!((mb >> i) & 1)) continue;
-            float4 v = fx ? make_float4(from_fx(r0[i].x), from_fx(r0[i].y), from_fx(r1[i].x), from_fx(r1[i].y)) : rf[i];
-            *reinterpret_cast<uint2 *>(fr + (base + i) * 2048) =
-                make_uint2(pack_f16(v.x * g[i].x, v.y * g[i].y), pack_f16(v.z * g[i].z, v.w * g[i].w));
+        for (int u = 0; u < B; ++u) {
+            const int i = i0 + u * NT;
+            if (i >= n) break;
+            const int c4 = i & 31, r = i >> 5, k = r / T, t = r - k * T;
+            const float4 v = a.fx ? make_float4(from_fx(x0[u].x), from_fx(x0[u].y), from_fx(x1[u].x), from_fx(x1[u].y))
+                                  : xf[u];
+            *reinterpret_cast<uint2 *>(fr + frag_off(__fns(mask, 0, k + 1), t, c4)) =
+                make_uint2(pack_f16(v.x * g[u].x, v.y * g[u].y), pack_f16(v.z * g[u].z, v.w * g[u].w));
         }
     }
 }
@@ -1062,37 +1095,47 @@ __device__ __noinline__ void build_h_frags(const RouteSm *rt, int ex, bool f32pa
         }
         return;
     }
-    const int s = c.tid >> 5, l = c.lane, n = l >> 2, q = l & 3;
-    const int col0 = frag_col(s, q, 0);
-    const long long *pa = base(n);
-    const float inv = n < c.T ? c.misc->inv_rms[1][n] : 0.f;
-    unsigned char *fr = c.sm + SM_SCRATCH + ((s >> 1) * 32 + l) * 16 + (s & 1) * 8;
+    // items (block, token, 4-column group), column group fastest: coalesced
+    // reads of whole rows of the gate/up accumulators
     const int nkb = m.I / 128;
-    for (int kb0 = 0; kb0 < nkb; kb0 += 4) {
-        longlong2 av[4][2], bv[4][2];
+    const uint32_t mask = nkb >= 32 ? 0xffffffffu : (1u << nkb) - 1u;
+    frag_zero_pad(c, mask);
+    unsigned char *fr = c.sm + SM_SCRATCH;
+    const int T = c.T, n = nkb * T * 32;
+    constexpr int B = 4, NT = MK_NCWARPS * 32;
+    for (int i0 = c.tid; i0 < n; i0 += B * NT) {
+        longlong2 av[B][2], bv[B][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (pa && kb0 + i < nkb) {
-                const longlong2 *pp = reinterpret_cast<const longlong2 *>(pa + (kb0 + i) * 128 + col0);
-                const longlong2 *pb = reinterpret_cast<const longlong2 *>(pa + m.I + (kb0 + i) * 128 + col0);
-                av[i][0] = __ldcg(pp);
-                av[i][1] = __ldcg(pp + 1);
-                bv[i][0] = __ldcg(pb);
-                bv[i][1] = __ldcg(pb + 1);
+        for (int u = 0; u < B; ++u) {
+            const int i = i0 + u * NT;
+            av[u][0] = av[u][1] = bv[u][0] = bv[u][1] = make_longlong2(0, 0);
+            if (i < n) {
+                const int c4 = i & 31, r = i >> 5, kb = r / T, t = r - kb * T;
+                const long long *pa = base(t);
+                if (pa) {
+                    const longlong2 *pp = reinterpret_cast<const longlong2 *>(pa + kb * 128 + 4 * c4);
+                    const longlong2 *pb = reinterpret_cast<const longlong2 *>(pa + m.I + kb * 128 + 4 * c4);
+                    av[u][0] = __ldcg(pp);
+                    av[u][1] = __ldcg(pp + 1);
+                    bv[u][0] = __ldcg(pb);
+                    bv[u][1] = __ldcg(pb + 1);
+                }
             }
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (kb0 + i >= nkb) break;
+        for (int u = 0; u < B; ++u) {
+            const int i = i0 + u * NT;
+            if (i >= n) break;
+            const int c4 = i & 31, r = i >> 5, kb = r / T, t = r - kb * T;
+            const float inv = c.misc->inv_rms[1][t];
             float h[4] = {0.f, 0.f, 0.f, 0.f};
-            if (pa) {
-                h[0] = silu_mul(from_fx(av[i][0].x) * inv, from_fx(bv[i][0].x) * inv);
-                h[1] = silu_mul(from_fx(av[i][0].y) * inv, from_fx(bv[i][0].y) * inv);
-                h[2] = silu_mul(from_fx(av[i][1].x) * inv, from_fx(bv[i][1].x) * inv);
-                h[3] = silu_mul(from_fx(av[i][1].y) * inv, from_fx(bv[i][1].y) * inv);
+            if (base(t)) {
+                h[0] = silu_mul(from_fx(av[u][0].x) * inv, from_fx(bv[u][0].x) * inv);
+                h[1] = silu_mul(from_fx(av[u][0].y) * inv, from_fx(bv[u][0].y) * inv);
+                h[2] = silu_mul(from_fx(av[u][1].x) * inv, from_fx(bv[u][1].x) * inv);
+                h[3] = silu_mul(from_fx(av[u][1].y) * inv, from_fx(bv[u][1].y) * inv);
             }
-            *reinterpret_cast<uint2 *>(fr + (kb0 + i) * 2048) =
-                make_uint2(pack_f16(h[0], h[1]), pack_f16(h[2], h[3]));
+            *reinterpret_cast<uint2 *>(fr + frag_off(kb, t, c4)) = make_uint2(pack_f16(h[0], h[1]), pack_f16(h[2], h[3]));
         }
     }
 }
