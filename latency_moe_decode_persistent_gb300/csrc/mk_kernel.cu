@@ -219,11 +219,20 @@ __device__ __forceinline__ long long to_fx(float v) {
     if (e == 0) r = 0;
     return (b >> 31) ? -(long long)r : (long long)r;
 }
-// from_fx: magnitude split into 32-bit halves, each converted exactly or
-// rounded once, then recombined (at most one extra rounding of the sum).
+// exact float of an integer u < 2^23: u is placed in the significand of 2^23
+// and 2^23 subtracted (FP32 and logic pipes only)
+__device__ __forceinline__ float u23_to_f(uint32_t u) {
+    return __uint_as_float(0x4b000000u | u) - 8388608.0f;
+}
+// from_fx: the magnitude's bits in three pieces of at most 22 bits, each
+// converted exactly, recombined with two fused multiply-adds (|v| < 2^63)
 __device__ __forceinline__ float from_fx(long long v) {
     const unsigned long long a = v < 0 ? 0ull - (unsigned long long)v : (unsigned long long)v;
-    const float f = fmaf(__uint2float_rn((uint32_t)a), 1.0f / MK_FX, __uint2float_rn((uint32_t)(a >> 32)));
+    const uint32_t lo = (uint32_t)a, hi = (uint32_t)(a >> 32);
+    const float f0 = u23_to_f(lo & 0x3fffffu);
+    const float f1 = u23_to_f((lo >> 22) | ((hi & 0xfffu) << 10));
+    const float f2 = u23_to_f(hi >> 12);
+    const float f = fmaf(f2, 4096.0f, fmaf(f1, 1.0f / 1024.0f, f0 * (1.0f / MK_FX)));
     return v < 0 ? -f : f;
 }
 __device__ __forceinline__ void red_add(long long *p, long long v) {
@@ -821,59 +830,50 @@ __device__ __forceinline__ uint32_t frag_off(int kb, int t, int c4) {
     const int q = c4 >> 3, sb = c4 & 1, x = (c4 >> 1) & 3;
     return kb * 2048 + ((((x - 2 * (q >> 1)) & 3) * 32 + 4 * t + q) << 4) + sb * 8;
 }
-// zero the fragment columns of tokens T..7 in the blocks of `mask` (the MMA
-// always reduces against all eight token columns)
-__device__ __forceinline__ void frag_zero_pad(const Ctx &c, uint32_t mask) {
-    const int np = MK_MAXT - c.T;
-    if (np <= 0) return;
-    unsigned char *fr = c.sm + SM_SCRATCH;
-    const int n = __popc(mask) * np * 32;
-    for (int i = c.tid; i < n; i += MK_NCWARPS * 32) {
-        const int c4 = i & 31, r = i >> 5, k = r / np, t = c.T + (r - k * np);
-        *reinterpret_cast<uint2 *>(fr + frag_off(__fns(mask, 0, k + 1), t, c4)) = make_uint2(0, 0);
-    }
-}
 // build f16 fragments for the 128-column blocks in `mask` (consumer threads).
-// Work items are (block, token, 4-column group) with the column group fastest,
-// so each warp reads whole contiguous rows of the source (full L2 lines) and
-// scatters the converted values into fragment order in shared memory; eight
-// items per thread are in flight before any is converted.
+// Thread (t, c4) = (tid / 32, tid % 32) converts columns 4*c4 .. 4*c4+3 of
+// token t in every block, so each warp reads one token's block row as whole
+// contiguous L2 lines; eight blocks are in flight before any is converted.
+// Tokens t >= T get zeros (the MMA reduces against all eight token columns).
 __device__ __noinline__ void build_frags(const ActSrc a, uint32_t mask) {
     const Ctx c = make_ctx();
     unsigned char *fr = c.sm + SM_SCRATCH;
-    frag_zero_pad(c, mask);
-    const int T = c.T, n = __popc(mask) * T * 32;
-    constexpr int B = 8, NT = MK_NCWARPS * 32;
-    for (int i0 = c.tid; i0 < n; i0 += B * NT) {
+    const int t = c.tid >> 5, c4 = c.lane;
+    const bool live = t < c.T;
+    const long long *fx = a.fx ? a.fx + (long long)t * a.stride + 4 * c4 : nullptr;
+    const float *f32 = a.f32 ? a.f32 + (long long)t * a.stride + 4 * c4 : nullptr;
+    const float *gm = a.gamma ? a.gamma + 4 * c4 : nullptr;
+    const uint32_t o_tc = frag_off(0, t, c4);
+    constexpr int B = 8;
+    uint32_t rest = mask;
+    while (rest) {
+        int kb[B];
         longlong2 x0[B], x1[B];
         float4 xf[B], g[B];
 #pragma unroll
         for (int u = 0; u < B; ++u) {
-            const int i = i0 + u * NT;
+            kb[u] = rest ? __ffs(rest) - 1 : -1;
+            rest &= rest - 1;
             x0[u] = x1[u] = make_longlong2(0, 0);
             xf[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             g[u] = make_float4(1.f, 1.f, 1.f, 1.f);
-            if (i < n) {
-                const int c4 = i & 31, r = i >> 5, k = r / T, t = r - k * T;
-                const int col = __fns(mask, 0, k + 1) * 128 + 4 * c4;
-                if (a.fx) {
-                    const longlong2 *pp = reinterpret_cast<const longlong2 *>(a.fx + (long long)t * a.stride + col);
-                    x0[u] = __ldcg(pp);
-                    x1[u] = __ldcg(pp + 1);
+            if (kb[u] >= 0 && live) {
+                const int col = kb[u] * 128;
+                if (fx) {
+                    x0[u] = __ldcg(reinterpret_cast<const longlong2 *>(fx + col));
+                    x1[u] = __ldcg(reinterpret_cast<const longlong2 *>(fx + col) + 1);
                 } else {
-                    xf[u] = __ldcg(reinterpret_cast<const float4 *>(a.f32 + (long long)t * a.stride + col));
+                    xf[u] = __ldcg(reinterpret_cast<const float4 *>(f32 + col));
                 }
-                if (a.gamma) g[u] = __ldg(reinterpret_cast<const float4 *>(a.gamma + col));
+                if (gm) g[u] = __ldg(reinterpret_cast<const float4 *>(gm + col));
             }
         }
 #pragma unroll
         for (int u = 0; u < B; ++u) {
-            const int i = i0 + u * NT;
-            if (i >= n) break;
-            const int c4 = i & 31, r = i >> 5, k = r / T, t = r - k * T;
-            const float4 v = a.fx ? make_float4(from_fx(x0[u].x), from_fx(x0[u].y), from_fx(x1[u].x), from_fx(x1[u].y))
-                                  : xf[u];
-            *reinterpret_cast<uint2 *>(fr + frag_off(__fns(mask, 0, k + 1), t, c4)) =
+            if (kb[u] < 0) break;
+            const float4 v = fx ? make_float4(from_fx(x0[u].x), from_fx(x0[u].y), from_fx(x1[u].x), from_fx(x1[u].y))
+                                : xf[u];
+            *reinterpret_cast<uint2 *>(fr + o_tc + kb[u] * 2048) =
                 make_uint2(pack_f16(v.x * g[u].x, v.y * g[u].y), pack_f16(v.z * g[u].z, v.w * g[u].w));
         }
     }
@@ -1095,47 +1095,39 @@ __device__ __noinline__ void build_h_frags(const RouteSm *rt, int ex, bool f32pa
         }
         return;
     }
-    // items (block, token, 4-column group), column group fastest: coalesced
-    // reads of whole rows of the gate/up accumulators
+    // thread (t, c4) converts columns 4*c4 .. 4*c4+3 of token t in every
+    // 128-column block: each warp reads one accumulator row as whole L2 lines
+    const int t = c.tid >> 5, c4 = c.lane;
+    const long long *pa = base(t);
+    const float inv = t < c.T ? c.misc->inv_rms[1][t] : 0.f;
+    unsigned char *fr = c.sm + SM_SCRATCH + frag_off(0, t, c4);
     const int nkb = m.I / 128;
-    const uint32_t mask = nkb >= 32 ? 0xffffffffu : (1u << nkb) - 1u;
-    frag_zero_pad(c, mask);
-    unsigned char *fr = c.sm + SM_SCRATCH;
-    const int T = c.T, n = nkb * T * 32;
-    constexpr int B = 4, NT = MK_NCWARPS * 32;
-    for (int i0 = c.tid; i0 < n; i0 += B * NT) {
+    constexpr int B = 4;
+    for (int kb0 = 0; kb0 < nkb; kb0 += B) {
         longlong2 av[B][2], bv[B][2];
 #pragma unroll
         for (int u = 0; u < B; ++u) {
-            const int i = i0 + u * NT;
             av[u][0] = av[u][1] = bv[u][0] = bv[u][1] = make_longlong2(0, 0);
-            if (i < n) {
-                const int c4 = i & 31, r = i >> 5, kb = r / T, t = r - kb * T;
-                const long long *pa = base(t);
-                if (pa) {
-                    const longlong2 *pp = reinterpret_cast<const longlong2 *>(pa + kb * 128 + 4 * c4);
-                    const longlong2 *pb = reinterpret_cast<const longlong2 *>(pa + m.I + kb * 128 + 4 * c4);
-                    av[u][0] = __ldcg(pp);
-                    av[u][1] = __ldcg(pp + 1);
-                    bv[u][0] = __ldcg(pb);
-                    bv[u][1] = __ldcg(pb + 1);
-                }
+            if (pa && kb0 + u < nkb) {
+                const longlong2 *pp = reinterpret_cast<const longlong2 *>(pa + (kb0 + u) * 128 + 4 * c4);
+                const longlong2 *pb = reinterpret_cast<const longlong2 *>(pa + m.I + (kb0 + u) * 128 + 4 * c4);
+                av[u][0] = __ldcg(pp);
+                av[u][1] = __ldcg(pp + 1);
+                bv[u][0] = __ldcg(pb);
+                bv[u][1] = __ldcg(pb + 1);
             }
         }
 #pragma unroll
         for (int u = 0; u < B; ++u) {
-            const int i = i0 + u * NT;
-            if (i >= n) break;
-            const int c4 = i & 31, r = i >> 5, kb = r / T, t = r - kb * T;
-            const float inv = c.misc->inv_rms[1][t];
+            if (kb0 + u >= nkb) break;
             float h[4] = {0.f, 0.f, 0.f, 0.f};
-            if (base(t)) {
+            if (pa) {
                 h[0] = silu_mul(from_fx(av[u][0].x) * inv, from_fx(bv[u][0].x) * inv);
                 h[1] = silu_mul(from_fx(av[u][0].y) * inv, from_fx(bv[u][0].y) * inv);
                 h[2] = silu_mul(from_fx(av[u][1].x) * inv, from_fx(bv[u][1].x) * inv);
                 h[3] = silu_mul(from_fx(av[u][1].y) * inv, from_fx(bv[u][1].y) * inv);
             }
-            *reinterpret_cast<uint2 *>(fr + frag_off(kb, t, c4)) = make_uint2(pack_f16(h[0], h[1]), pack_f16(h[2], h[3]));
+            *reinterpret_cast<uint2 *>(fr + (kb0 + u) * 2048) = make_uint2(pack_f16(h[0], h[1]), pack_f16(h[2], h[3]));
         }
     }
 }
@@ -1989,6 +1981,7 @@ __device__ __noinline__ void consumer() {
         // ---- router + shared expert gate/up, then routed gate/up
         {
             ActSrc a{m.res, nullptr, m.H, L.moe_norm};
+            mark(c, ST_ROUTER * 16 + 8);
             if (f32path) build_act32(a, m.H);
             else build_frags(a, allH);
             ssq_block(c, 1);
