@@ -564,10 +564,17 @@ __device__ __forceinline__ MatR mat_regs(const DMat &d) {
 // Walks the tiles of one stage that belong to this CTA, in (expert slot,
 // matrix, 128-row group, 128-byte column chunk) order.  Descriptors are read
 // once per stage; the position advances with counters, no divisions.
+// Walks the tiles of one stage that belong to this CTA.  The router, shared
+// gate/up and routed gate/up stages are ordered column chunk first (1024
+// input columns), then (expert slot, matrix, 256-row group, 128-byte column
+// piece): every CTA then works inside one or two chunks and needs only those
+// columns of its input.  Other stages are one chunk wide.  Descriptors are
+// read once per stage; the position advances with counters, no divisions.
 struct StageIter {
     MatR m0, m1;          // matrix 0 / 1 (gate/up pairs; routed/shared down)
     int n_rg, n_kc, nmat, nex, nd;
     int ex, mat, rg, kc, n;
+    int kc0, kcn;         // first column piece of the current chunk; pieces per chunk
     int st;
     const int *dlist;
     __device__ __forceinline__ const MatR &cur() const {
@@ -576,19 +583,39 @@ struct StageIter {
     __device__ __forceinline__ int expert() const {
         return (st == ST_EXPA || (st == ST_EXPB && ex < nd)) ? dlist[ex] : 0;
     }
+    __device__ __forceinline__ bool item_start() const { return kc == kc0; }
     __device__ __forceinline__ void advance() {
-        if (++kc == n_kc) {
-            kc = 0;
+        if (++kc == kc0 + kcn) {
+            kc = kc0;
             if (++rg == n_rg) {
                 rg = 0;
                 if (++mat == nmat) {
                     mat = 0;
-                    ++ex;
+                    if (++ex == nex) {
+                        ex = 0;
+                        kc0 += kcn;
+                        kc = kc0;
+                    }
                 }
             }
         }
     }
 };
+
+__device__ __forceinline__ bool chunk_major(int st) { return st == ST_ROUTER || st == ST_SHA || st == ST_EXPA; }
+
+// 128-column blocks of the input chunks this CTA works on in the chunk-major
+// stages (input width `cols`): chunks nch*cta/G .. ceil(nch*(cta+1)/G) - 1,
+// whatever the number of tiles per chunk
+__device__ uint32_t chunk_kb_mask(const Ctx &c, int cols) {
+    const uint32_t all = 0xffffffffu >> (32 - cols / 128);
+    if (cols % 1024) return all;
+    const int nch = cols / 1024;
+    const int c0 = nch * c.cta / c.G, c1 = (nch * (c.cta + 1) + c.G - 1) / c.G - 1;
+    uint32_t msk = 0;
+    for (int ch = c0; ch <= c1 && ch < nch; ++ch) msk |= 0xffu << (8 * ch);
+    return msk & all;
+}
 
 __device__ void stage_iter(StageIter &it, const Ctx &c, int st, const DLayer &L, const RouteSm *rt) {
     const DModel &m = *c.m;
@@ -626,16 +653,31 @@ __device__ void stage_iter(StageIter &it, const Ctx &c, int st, const DLayer &L,
                      st == ST_LM ? m.lm : st == ST_SHA ? L.s1 : st == ST_EXPA ? L.w1 : L.w2;
     it.n_rg = d0.n_rg;
     it.n_kc = d0.n_kc;
-    const int per_mat = it.n_rg * it.n_kc, per_ex = it.nmat * per_mat;
+    it.kcn = (chunk_major(st) && d0.cols % 1024 == 0) ? 8 * d0.es : it.n_kc;
+    const int nch = it.n_kc / it.kcn;
+    const int per_mat = it.n_rg * it.kcn, per_ex = it.nmat * per_mat, per_ch = it.nex * per_ex;
     int b, e;
-    split_range(it.nex * per_ex, c.G, c.cta, b, e);
+    if (st == ST_EXPA || st == ST_EXPB) {
+        // whole items only: an item's partial sum is then formed by one CTA in
+        // a fixed tile order whatever the number of routed experts, so the
+        // step's result for a token does not depend on the other tokens of
+        // the block (batch invariance); per-CTA counts differ by one item
+        split_range(nch * per_ch / it.kcn, c.G, c.cta, b, e);
+        b *= it.kcn;
+        e *= it.kcn;
+    } else {
+        split_range(nch * per_ch, c.G, c.cta, b, e);
+    }
     it.n = e - b;
-    it.ex = b / per_ex;
-    int r = b - it.ex * per_ex;
-    it.mat = r / per_mat;
+    const int ch = per_ch ? b / per_ch : 0;
+    int r = b - ch * per_ch;
+    it.ex = per_ex ? r / per_ex : 0;
+    r -= it.ex * per_ex;
+    it.mat = per_mat ? r / per_mat : 0;
     r -= it.mat * per_mat;
-    it.rg = r / it.n_kc;
-    it.kc = r - it.rg * it.n_kc;
+    it.rg = r / it.kcn;
+    it.kc0 = ch * it.kcn;
+    it.kc = it.kc0 + (r - it.rg * it.kcn);
 }
 
 // ------------------------------------------------------------------ producer
@@ -1132,6 +1174,7 @@ __device__ __noinline__ void build_h_frags(const RouteSm *rt, int ex, bool f32pa
     }
 }
 
+
 // consume this CTA's tiles of one GEMV stage
 __device__ __forceinline__ void flush_item(const Ctx &c, int st, int ex, int mat, int rg, const MatR &d,
                                            const RouteSm *rt, const float *acc) {
@@ -1139,7 +1182,6 @@ __device__ __forceinline__ void flush_item(const Ctx &c, int st, int ex, int mat
     if (d.dtype == MK_DT_F32) flush_f32(c, g, rg * 256 + c.warp * 32, acc);
     else flush_mma(c, g, rg * 256 + c.warp * 32, acc);
 }
-
 // consume this CTA's tiles of one GEMV stage
 __device__ __noinline__ uint32_t cons_gemv(int st, const DLayer *Lp, const RouteSm *rt, uint32_t ci) {
     const Ctx c = make_ctx();
@@ -1157,7 +1199,7 @@ __device__ __noinline__ uint32_t cons_gemv(int st, const DLayer *Lp, const Route
     const int ntiles = it.n;
     for (int k = 0; it.n > 0; --it.n, it.advance(), ++k) {
         const MatR &d = it.cur();
-        if (k == 0 || it.kc == 0) {  // a new (expert slot, matrix, row group) item starts
+        if (k == 0 || it.item_start()) {  // a new (expert slot, matrix, row group) item starts
             if (k > 0) {
                 flush_item(c, st, cex, cmat, crg, cmat || (st == ST_EXPB && cex >= it.nd) ? it.m1 : it.m0, rt, acc);
 #pragma unroll
@@ -1983,7 +2025,7 @@ __device__ __noinline__ void consumer() {
             ActSrc a{m.res, nullptr, m.H, L.moe_norm};
             mark(c, ST_ROUTER * 16 + 8);
             if (f32path) build_act32(a, m.H);
-            else build_frags(a, allH);
+            else build_frags(a, chunk_kb_mask(c, m.H));
             ssq_block(c, 1);
             bar_consumers();
             mark(c, ST_ROUTER * 16 + 0);
