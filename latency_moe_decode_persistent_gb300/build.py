@@ -7,7 +7,10 @@ from concurrent.futures import ThreadPoolExecutor
 HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libmk.so")
-SOURCES = ["mk_kernel.cu", "mk_api.cu"]
+# (source, object, extra flags): the kernel is built once per model class
+SOURCES = [("mk_kernel.cu", "mk_kernel_lp.o", ["-DMK_F32_MODEL=0"]),
+           ("mk_kernel.cu", "mk_kernel_f32.o", ["-DMK_F32_MODEL=1"]),
+           ("mk_api.cu", "mk_api.o", [])]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 
@@ -25,9 +28,10 @@ def build(verbose: bool = False, extra=()) -> str:
     objdir = os.path.join(HERE, "_build")
     os.makedirs(objdir, exist_ok=True)
 
-    def comp(src):
-        obj = os.path.join(objdir, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+    def comp(spec):
+        src, o, defs = spec
+        obj = os.path.join(objdir, o)
+        cmd = [nvcc, *ARCH, *FLAGS, *defs, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, r.stdout, r.stderr))

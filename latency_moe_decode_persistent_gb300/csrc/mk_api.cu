@@ -12,10 +12,10 @@
 
 #include "mk_internal.h"
 
-int mk_kernel_max_blocks(size_t smem);
 
 struct mk_state {
     mk_model_desc desc;
+    bool f32 = false;                   // all-fp32 model: the FFMA kernel build
     int device = 0, grid = 0;
     size_t smem = 0;
     // device allocations
@@ -148,11 +148,13 @@ mk_status check_desc(mk_state *st, const mk_model_desc *d) {
     int G = d->n_q_heads / d->n_kv_heads;
     if (G * d->max_T > MK_MAXROWS) return fail(st, MK_ERR_UNSUPPORTED, "(n_q_heads/n_kv_heads)*max_T > 64");
     if (d->kv_dtype != MK_DT_F32 && d->kv_dtype != MK_DT_BF16) return fail(st, MK_ERR_UNSUPPORTED, "kv_dtype must be F32 or BF16");
-    int kv_es = dt_size(d->kv_dtype);
-    bool mma_att = d->kv_dtype == MK_DT_BF16 && d->head_dim == 128;
-    if (!mma_att) {
-        if (d->head_dim != 64) return fail(st, MK_ERR_UNSUPPORTED, "an fp32 KV cache (or head_dim 64) needs head_dim 64");
-        if (G * d->max_T > 16) return fail(st, MK_ERR_UNSUPPORTED, "this KV layout supports (n_q_heads/n_kv_heads)*T <= 16");
+    // all-fp32 models run the FFMA kernel (attention over head_dim 64, f32 or
+    // bf16 KV); bf16 / FP8 models run the tensor-core kernel (head_dim 128, bf16 KV)
+    if (d->weight_dtype == MK_DT_F32) {
+        if (d->head_dim != 64) return fail(st, MK_ERR_UNSUPPORTED, "fp32 weights need head_dim 64");
+        if (G * d->max_T > 16) return fail(st, MK_ERR_UNSUPPORTED, "fp32 weights support (n_q_heads/n_kv_heads)*T <= 16");
+    } else if (d->kv_dtype != MK_DT_BF16 || d->head_dim != 128) {
+        return fail(st, MK_ERR_UNSUPPORTED, "bf16 / FP8 weights need a bf16 KV cache and head_dim 128");
     }
     if (d->weight_dtype < 0 || d->weight_dtype > 2) return fail(st, MK_ERR_UNSUPPORTED, "weight_dtype");
     if ((d->weight_dtype == MK_DT_F32) != (d->router_dtype == MK_DT_F32))
@@ -221,8 +223,9 @@ mk_status mk_create(const mk_model_desc *desc, const mk_weights *w, mk_state **o
     st->smem = SM_TOTAL + 1024;
     if (st->smem > (size_t)prop.sharedMemPerBlockOptin)
         return bail(fail(st, MK_ERR_UNSUPPORTED, "needs %zu bytes of shared memory per block", st->smem));
-    if (mk_kernel_setup(st->smem) != cudaSuccess) return bail(fail(st, MK_ERR_CUDA, "cudaFuncSetAttribute"));
-    int per_sm = mk_kernel_max_blocks(st->smem);
+    st->f32 = d.weight_dtype == MK_DT_F32;
+    if (mk_kernel_setup(st->smem, st->f32) != cudaSuccess) return bail(fail(st, MK_ERR_CUDA, "cudaFuncSetAttribute"));
+    int per_sm = mk_kernel_max_blocks(st->smem, st->f32);
     if (per_sm < 1) return bail(fail(st, MK_ERR_UNSUPPORTED, "persistent CTA does not fit on an SM"));
     st->grid = prop.multiProcessorCount;  // one persistent CTA per SM
 
@@ -386,7 +389,7 @@ static mk_status launch(mk_state *st, Params &p, void *stream) {
     p.kpool = st->d_kpool;
     p.vpool = st->d_vpool;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = mk_launch(p, st->grid, st->smem, s);
+    cudaError_t e = mk_launch(p, st->grid, st->smem, s, st->f32);
     if (e != cudaSuccess) return fail(st, MK_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
     st->last_stream = s;
     st->launched = true;
@@ -549,8 +552,10 @@ mk_status noalloc_setup(mk_state *st, int dev, NoallocDevice **out) {
         if (prop.major != 10 || prop.minor != 3)
             return fail(st, MK_ERR_UNSUPPORTED, "built for compute capability 10.3, device is %d.%d", prop.major, prop.minor);
         const size_t smem = SM_TOTAL + 1024;
-        if (mk_kernel_setup(smem) != cudaSuccess) return fail(st, MK_ERR_CUDA, "cudaFuncSetAttribute");
-        if (mk_kernel_max_blocks(smem) < 1) return fail(st, MK_ERR_UNSUPPORTED, "persistent CTA does not fit on an SM");
+        for (int f = 0; f < 2; ++f) {
+            if (mk_kernel_setup(smem, f != 0) != cudaSuccess) return fail(st, MK_ERR_CUDA, "cudaFuncSetAttribute");
+            if (mk_kernel_max_blocks(smem, f != 0) < 1) return fail(st, MK_ERR_UNSUPPORTED, "persistent CTA does not fit on an SM");
+        }
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
@@ -745,7 +750,7 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     p.hidden_out = hidden_out;
     p.out_idx = out_topk_idx;
     p.out_w = out_topk_w;
-    cudaError_t e = mk_launch(p, nd->grid, nd->smem, s);
+    cudaError_t e = mk_launch(p, nd->grid, nd->smem, s, d.weight_dtype == MK_DT_F32);
     if (e != cudaSuccess) return ret(fail(st, MK_ERR_CUDA, "launch: %s", cudaGetErrorString(e)));
     if (out_status)
         CKN(cudaMemcpyAsync(out_status, base + o_ctrl + offsetof(Ctrl, status), sizeof(int32_t),

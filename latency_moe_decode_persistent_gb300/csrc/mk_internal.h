@@ -123,5 +123,20 @@ struct Params {
     unsigned long long *marks;         // [G][MK_MARKS][2] (event id, time) or null
 };
 
-cudaError_t mk_launch(const Params &p, int grid, size_t smem, cudaStream_t s);
-cudaError_t mk_kernel_setup(size_t smem);
+// one kernel per model class (mk_kernel.cu compiled twice): _f32 for all-fp32
+// models, _lp for bf16 / FP8 models
+cudaError_t mk_launch_f32(const Params &p, int grid, size_t smem, cudaStream_t s);
+cudaError_t mk_kernel_setup_f32(size_t smem);
+int mk_kernel_max_blocks_f32(size_t smem);
+cudaError_t mk_launch_lp(const Params &p, int grid, size_t smem, cudaStream_t s);
+cudaError_t mk_kernel_setup_lp(size_t smem);
+int mk_kernel_max_blocks_lp(size_t smem);
+inline cudaError_t mk_launch(const Params &p, int grid, size_t smem, cudaStream_t s, bool f32) {
+    return f32 ? mk_launch_f32(p, grid, smem, s) : mk_launch_lp(p, grid, smem, s);
+}
+inline cudaError_t mk_kernel_setup(size_t smem, bool f32) {
+    return f32 ? mk_kernel_setup_f32(smem) : mk_kernel_setup_lp(smem);
+}
+inline int mk_kernel_max_blocks(size_t smem, bool f32) {
+    return f32 ? mk_kernel_max_blocks_f32(smem) : mk_kernel_max_blocks_lp(smem);
+}

@@ -35,7 +35,18 @@
 
 #include "mk_internal.h"
 
+// This file is compiled twice: with MK_F32_MODEL=1 for all-fp32 models (FFMA
+// GEMV tiles, FFMA attention over head_dim 64) and with MK_F32_MODEL=0 for
+// bf16 / FP8 models (tensor-core tiles and attention).  Each kernel then holds
+// only the code paths its models take, which keeps it small for the
+// instruction cache: most of the step's code runs once per layer.
+#ifndef MK_F32_MODEL
+#define MK_F32_MODEL 0
+#endif
+
 namespace {
+
+constexpr bool kF32 = MK_F32_MODEL != 0;
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t sa(const void *p) {
@@ -1117,7 +1128,9 @@ __device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + 
 
 // expert intermediate h = silu(a/rms) * (b/rms) of one routed expert (or the
 // shared one) as f16 fragments; eight blocks of loads are issued at once
-__device__ __noinline__ void build_h_frags(const RouteSm *rt, int ex, bool f32path) {
+__device__ __noinline__ void build_h_frags(const RouteSm *rt, int ex, bool f32path_) {
+    constexpr bool f32path = kF32;
+    (void)f32path_;
     const Ctx c = make_ctx();
     const DModel &m = *c.m;
     const bool shared = ex >= rt->nd;
@@ -1179,7 +1192,7 @@ __device__ __noinline__ void build_h_frags(const RouteSm *rt, int ex, bool f32pa
 __device__ __forceinline__ void flush_item(const Ctx &c, int st, int ex, int mat, int rg, const MatR &d,
                                            const RouteSm *rt, const float *acc) {
     const Tgt g = make_tgt(c, st, ex, mat, d.rows, rt);
-    if (d.dtype == MK_DT_F32) flush_f32(c, g, rg * 256 + c.warp * 32, acc);
+    if (kF32 && d.dtype == MK_DT_F32) flush_f32(c, g, rg * 256 + c.warp * 32, acc);
     else flush_mma(c, g, rg * 256 + c.warp * 32, acc);
 }
 // consume this CTA's tiles of one GEMV stage
@@ -1210,7 +1223,7 @@ __device__ __noinline__ uint32_t cons_gemv(int st, const DLayer *Lp, const Route
             crg = it.rg;
             if (st == ST_EXPB && it.ex != last_hex) {
                 bar_consumers();
-                build_h_frags(rt, it.ex, d.dtype == MK_DT_F32);
+                build_h_frags(rt, it.ex, kF32);
                 bar_consumers();
                 last_hex = it.ex;
             }
@@ -1220,7 +1233,7 @@ __device__ __noinline__ uint32_t cons_gemv(int st, const DLayer *Lp, const Route
         if (mbar_wait(&full[slot], (ci / MK_RING) & 1, c, 200 + st)) {
             unsigned long long cy2 = prof ? clock64() : 0;
             if (k == 0) mark(c, st * 16 + 1);
-            if (d.dtype == MK_DT_F32) tile_f32(c, d.cols, slot, it.kc, acc);
+            if (kF32 && d.dtype == MK_DT_F32) tile_f32(c, d.cols, slot, it.kc, acc);
             else tile_mma(c, d.dtype, slot, it.kc, acc);
             if (prof) {
                 unsigned long long cy3 = clock64();
@@ -1716,7 +1729,7 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     const DModel &m = *c.m;
     const AttUnit u = att_unit(c);
     const int G = m.Hq / m.Hkv, R = G * c.T;
-    const bool mma_path = (m.kv_es == 2 && m.d == 128);
+    constexpr bool mma_path = !kF32;
     const int nbox = (m.d * m.kv_es) / 128, bs = m.P * 128;
     const int D2 = m.d + 2;
     compute_inv_rms(c, 0);
@@ -1956,7 +1969,7 @@ __device__ __noinline__ void consumer() {
     const DModel &m = *c.m;
     const Params &p = *c.p;
     uint32_t ci = 0;
-    const bool f32path = m.wdt == MK_DT_F32;
+    constexpr bool f32path = kF32;
     const uint32_t allH = 0xffffffffu >> (32 - m.H / 128);
     int nl = p.mode ? 1 : m.L;
     // zero the accumulators, load the residual stream
@@ -2264,16 +2277,22 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_step_kernel(const __grid_con
 
 }  // namespace
 
-cudaError_t mk_kernel_setup(size_t smem) {
+#if MK_F32_MODEL
+#define MK_SFX(x) x##_f32
+#else
+#define MK_SFX(x) x##_lp
+#endif
+
+cudaError_t MK_SFX(mk_kernel_setup)(size_t smem) {
     return cudaFuncSetAttribute(mk_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
 
-cudaError_t mk_launch(const Params &p, int grid, size_t smem, cudaStream_t s) {
+cudaError_t MK_SFX(mk_launch)(const Params &p, int grid, size_t smem, cudaStream_t s) {
     void *args[] = {(void *)&p};
     return cudaLaunchCooperativeKernel((const void *)mk_step_kernel, dim3(grid), dim3(MK_THREADS), args, smem, s);
 }
 
-int mk_kernel_max_blocks(size_t smem) {
+int MK_SFX(mk_kernel_max_blocks)(size_t smem) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mk_step_kernel, MK_THREADS, smem) != cudaSuccess) return -1;
     return n;

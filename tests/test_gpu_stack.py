@@ -129,3 +129,22 @@ def test_full_43_layer_stack():
         assert err < gc.TOL[synth.WDT_FP8], err
     finally:
         b.close()
+
+
+def test_block_verification_is_batch_invariant():
+    """Block verification = sequential decode, bit for bit on the GPU: the logits
+    of position i from a step over the first i+1 tokens equal row i of the full
+    step (the work split of the routed-expert stages changes with the set of
+    distinct experts, so this pins that a token's result does not depend on the
+    other tokens of the block).  The pages' greedy byte-for-byte gate, adapted."""
+    cfg = mini_stack(seed=51)
+    b = gc.Built(cfg)
+    try:
+        toks = [int(v) for v in np.random.default_rng(9).integers(0, cfg.vocab, cfg.T)]
+        full, _, am_full, _ = b.step(toks, trace=False)
+        for n in range(1, cfg.T):
+            part, _, am, _ = b.step(toks[:n], trace=False)
+            assert torch.equal(part, full[:n]), "prefix of %d tokens differs" % n
+            assert torch.equal(am, am_full[:n])
+    finally:
+        b.close()
