@@ -21,7 +21,7 @@
 #define MK_MAXD (MK_MAXT * MK_MAXK)      // distinct experts per layer
 #define MK_MAXROWS 64                    // (q heads per kv head) x T
 #define MK_MAXSPLIT 160                  // attention splits per kv head
-#define MK_ATT_MIN_PAGES 2               // KV pages per attention split, at least
+#define MK_ATT_MIN_PAGES 1               // KV pages per attention split, at least
 #define MK_MARKS 1024                    // intra-stage trace events per CTA
 #define MK_FX 4294967296.0f              // fixed-point scale of the cross-CTA accumulators
 

@@ -270,7 +270,8 @@ struct RouteSm {
 struct MiscSm {
     int abort;
     int gs_ok;
-    int emask[16];
+    int emask[16];               // routed experts of the block (bit set)
+    int epre[16];                // routed experts in the mask words before each word
     float inv_rms[3][MK_MAXT];   // attention, moe, final
     int distinct_total;
     int valid, ctx, nsplit;
@@ -1291,13 +1292,18 @@ __device__ void compute_inv_rms(const Ctx &c, int which) {
 }
 
 // ------------------------------------------------------------------ routing
-__device__ __forceinline__ unsigned long long key64(float key, int e) {
+// Selection key of expert e: the order-preserving bit pattern of s + b with
+// its 9 lowest significand bits replaced by 511 - e, so that larger keys win
+// and, between keys within 2^-14 relative of each other, the lower expert
+// index wins.  (Routing is compared exactly only where the 8th and 9th keys
+// differ by more than 1e-3.)
+__device__ __forceinline__ uint32_t key32(float key, int e) {
     uint32_t b = __float_as_uint(key);
     b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    return ((unsigned long long)b << 32) | (0xffffffffu - (uint32_t)e);
+    return (b & ~0x1ffu) | (uint32_t)(511 - e);
 }
 // sort 16 keys descending (bitonic network, registers)
-__device__ __forceinline__ void bitonic16_desc(unsigned long long *v) {
+__device__ __forceinline__ void bitonic16_desc(uint32_t *v) {
 #pragma unroll
     for (int k = 2; k <= 16; k <<= 1) {
 #pragma unroll
@@ -1306,32 +1312,40 @@ __device__ __forceinline__ void bitonic16_desc(unsigned long long *v) {
             for (int i = 0; i < 16; ++i) {
                 int l = i ^ j;
                 if (l > i) {
-                    bool desc = (i & k) == 0;
-                    unsigned long long a = v[i], b = v[l];
-                    bool sw = desc ? (a < b) : (a > b);
-                    v[i] = sw ? b : a;
-                    v[l] = sw ? a : b;
+                    const uint32_t a = v[i], b = v[l];
+                    const bool desc = (i & k) == 0;
+                    v[i] = desc ? max(a, b) : min(a, b);
+                    v[l] = desc ? min(a, b) : max(a, b);
                 }
             }
         }
     }
 }
 
-// top-K of each token's sigmoid scores + bias; weights from the unbiased scores
+// Routing of the block, every CTA redundantly.  Warp t < T takes token t:
+// one batch of loads brings its sum-of-squares partials (for the MoE RMSNorm)
+// and its router logits; keys s + b (selection bias) are sorted 16 per lane
+// by a bitonic network and merged across the warp to the top K; the weights
+// are the unbiased scores of the chosen experts (taken from their owner lanes
+// by shuffle) normalised to 1.  The distinct experts of the block and each
+// (expert slot, token) pair then come from a bit mask and a prefix count.
 __device__ __noinline__ void route_layer(const DLayer *Lp, RouteSm *rt) {
     const Ctx c = make_ctx();
     const DLayer &L = *Lp;
     const DModel &m = *c.m;
     mark(c, ST_EXPA * 16 + 4);
+    if (c.tid < 16) c.misc->emask[c.tid] = 0;
+    for (int i = c.tid; i < MK_MAXD * MK_MAXT / 4; i += MK_NCWARPS * 32)
+        reinterpret_cast<int *>(&rt->dslot[0][0])[i] = -1;
+    bar_consumers();
     if (c.warp < c.T) {
         const int t = c.warp;
-        const float inv = c.misc->inv_rms[1][t];
-        unsigned long long v[16];
+        float sq = c.lane < m.H / 128 ? __ldcg(m.ssq + (MK_MAXKB + c.lane) * MK_MAXT + t) : 0.f;
         long long raw[16];
         float bias[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {  // phase 1: all loads in flight
-            int e = c.lane + 32 * i;
+        for (int i = 0; i < 16; ++i) {
+            const int e = c.lane + 32 * i;
             raw[i] = 0;
             bias[i] = 0.f;
             if (e < m.E) {
@@ -1340,97 +1354,89 @@ __device__ __noinline__ void route_layer(const DLayer *Lp, RouteSm *rt) {
             }
         }
 #pragma unroll
+        for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        const float inv = rsqrtf(sq / (float)m.H + m.eps);
+        if (c.lane == 0) c.misc->inv_rms[1][t] = inv;
+        float sg[16];
+        uint32_t v[16];
+#pragma unroll
         for (int i = 0; i < 16; ++i) {
-            int e = c.lane + 32 * i;
-            v[i] = 0ull;
-            if (e < m.E) {
-                float lg = from_fx(raw[i]) * inv;
-                float s = 1.f / (1.f + expf(-lg));
-                v[i] = key64(s + bias[i], e);
-            }
-        }
-        if (c.warp == 0 && c.lane == 0 && c.p->marks) {
-            unsigned long long *e = c.p->marks + ((long long)c.cta * MK_MARKS + (MK_MARKS - 72)) * 2;
-            e[0] = ST_EXPA * 16 + 5;
-            e[1] = gtimer();
+            const int e = c.lane + 32 * i;
+            sg[i] = 1.f / (1.f + expf(-from_fx(raw[i]) * inv));
+            v[i] = e < m.E ? key32(sg[i] + bias[i], e) : 0u;
         }
         bitonic16_desc(v);
         // bitonic merge of the lanes' sorted top-8 lists
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            unsigned long long pv[8];
+            uint32_t pv[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) pv[i] = __shfl_xor_sync(0xffffffffu, v[i], o);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = v[i] > pv[7 - i] ? v[i] : pv[7 - i];
+            for (int i = 0; i < 8; ++i) v[i] = max(v[i], pv[7 - i]);
 #pragma unroll
-            for (int j = 4; j > 0; j >>= 1) {
+            for (int jj = 4; jj > 0; jj >>= 1) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    if ((i & j) == 0) {
-                        unsigned long long a = v[i], b = v[i + j];
-                        v[i] = a > b ? a : b;
-                        v[i + j] = a > b ? b : a;
+                    if ((i & jj) == 0) {
+                        const uint32_t a = v[i], b = v[i + jj];
+                        v[i] = max(a, b);
+                        v[i + jj] = min(a, b);
                     }
                 }
             }
         }
-        // lanes 0..K-1 take entry `lane`
-        unsigned long long mine = 0;
+        // lane j < K takes entry j of the merged list
+        uint32_t mine = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             if (i == c.lane) mine = v[i];
-        int e = (int)(0xffffffffu - (uint32_t)(mine & 0xffffffffu));
+        const int e = 511 - (int)(mine & 0x1ffu);
         float s = 0.f;
-        if (c.lane < m.K) {
-            float lg = from_fx(__ldcg(m.rlog + (long long)t * m.E + e)) * inv;
-            s = 1.f / (1.f + expf(-lg));
+        for (int j = 0; j < m.K; ++j) {
+            const int ej = __shfl_sync(0xffffffffu, e, j);
+            float val = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (i == (ej >> 5)) val = sg[i];
+            val = __shfl_sync(0xffffffffu, val, ej & 31);
+            if (c.lane == j) s = val;
         }
-        float sum = s;
+        float sum = c.lane < m.K ? s : 0.f;
 #pragma unroll
         for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         if (c.lane < m.K) {
             rt->idx[t][c.lane] = e;
             rt->w[t][c.lane] = s / sum;
+            atomicOr(&c.misc->emask[e >> 5], 1 << (e & 31));
         }
     }
-    if (c.tid < 16) c.misc->emask[c.tid] = 0;
     bar_consumers();
     mark(c, ST_EXPA * 16 + 6);
     if (c.warp == 0) {
-        for (int i = c.lane; i < c.T * m.K; i += 32) {
-            int e = rt->idx[i / m.K][i % m.K];
-            atomicOr(&c.misc->emask[e >> 5], 1 << (e & 31));
-        }
-        __syncwarp();
-        int cnt = c.lane < 16 ? __popc(c.misc->emask[c.lane]) : 0;
+        const int cnt = c.lane < 16 ? __popc(c.misc->emask[c.lane]) : 0;
         int pre = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, pre, o);
+            const int y = __shfl_up_sync(0xffffffffu, pre, o);
             if (c.lane >= o) pre += y;
         }
-        int total = __shfl_sync(0xffffffffu, pre, 31);
         if (c.lane < 16) {
             int pos = pre - cnt;
+            c.misc->epre[c.lane] = pos;
             uint32_t w = c.misc->emask[c.lane];
             while (w) {
-                int bit = __ffs(w) - 1;
+                rt->dlist[pos++] = c.lane * 32 + __ffs(w) - 1;
                 w &= w - 1;
-                rt->dlist[pos++] = c.lane * 32 + bit;
             }
         }
-        if (c.lane == 0) rt->nd = total;
-        for (int i = c.lane; i < MK_MAXD * MK_MAXT; i += 32) (&rt->dslot[0][0])[i] = -1;
-        __syncwarp();
-        for (int i = c.lane; i < c.T * m.K; i += 32) {
-            int t = i / m.K, j = i % m.K, e = rt->idx[t][j];
-            int wd = e >> 5;
-            int pos = 0;
-            for (int k = 0; k < wd; ++k) pos += __popc(c.misc->emask[k]);
-            pos += __popc(c.misc->emask[wd] & ((1u << (e & 31)) - 1));
-            rt->dslot[pos][t] = (signed char)j;
-        }
+        if (c.lane == 31) rt->nd = pre;
+    }
+    bar_consumers();
+    if (c.warp < c.T && c.lane < m.K) {
+        const int t = c.warp, e = rt->idx[t][c.lane], wd = e >> 5;
+        const int pos = c.misc->epre[wd] + __popc(c.misc->emask[wd] & ((1u << (e & 31)) - 1u));
+        rt->dslot[pos][t] = (signed char)c.lane;
     }
     bar_consumers();
 }
@@ -1912,45 +1918,52 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     split_range(R, c.nsplit, u.s, r0, r1);
     const int nr = r1 - r0, ns = c.nsplit;
     const float *pbase = m.att_part + (long long)(u.g * MK_MAXSPLIT) * MK_MAXROWS * D2;
-    // per-split weights exp2(m_s - M) / L of my rows, in scratch
-    float *wts = reinterpret_cast<float *>(scr);            // [nr][ns]
-    for (int i = c.tid; i < nr * ns; i += MK_NCWARPS * 32) {
-        int rr = i / ns, sp = i - rr * ns;
-        const float *pp = pbase + ((long long)sp * MK_MAXROWS + r0 + rr) * D2 + m.d;
-        wts[i] = __ldcg(pp);                                 // m
-        wts[nr * ns + i] = __ldcg(pp + 1);                   // l
-    }
-    bar_consumers();
-    if (c.tid < nr) {
-        float *mw = wts + c.tid * ns, *lw = wts + nr * ns + c.tid * ns;
-        float mx = -1e30f;
-        for (int sp = 0; sp < ns; ++sp) mx = fmaxf(mx, mw[sp]);
-        float lsum = 0.f;
-        for (int sp = 0; sp < ns; ++sp) {
-            float a = exp2f(mw[sp] - mx);
-            mw[sp] = a;
-            lsum += a * lw[sp];
-        }
-        float il = 1.f / lsum;
-        for (int sp = 0; sp < ns; ++sp) mw[sp] *= il;
-    }
-    bar_consumers();
-    for (int i = c.tid; i < nr * m.d; i += MK_NCWARPS * 32) {
-        int rr = i / m.d, dd = i - rr * m.d;
-        const float *w = wts + rr * ns;
-        const float *pp = pbase + (long long)(r0 + rr) * D2 + dd;
-        float acc = 0.f;
-        int sp = 0;
-        for (; sp + 8 <= ns; sp += 8) {
-            float v[8];
+    // log-sum-exp merge of my rows: thread (row, column pair) reads every
+    // split's (m, l) and partial output in chunks of 16 splits, all loads of a
+    // chunk in flight at once, and folds them with the running maximum
+    const int hp = m.d / 2;
+    for (int item = c.tid; item < nr * hp; item += MK_NCWARPS * 32) {
+        const int rr = item / hp, dp = item - rr * hp;
+        const float *prow = pbase + (long long)(r0 + rr) * D2;
+        const long long sstr = (long long)MK_MAXROWS * D2;
+        float M = -1e30f, lsum = 0.f;
+        float2 acc = make_float2(0.f, 0.f);
+        constexpr int CH = 16;
+        for (int sp0 = 0; sp0 < ns; sp0 += CH) {
+            float mv[CH], lv[CH];
+            float2 av[CH];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = __ldcg(pp + (long long)(sp + k) * MK_MAXROWS * D2);
+            for (int k = 0; k < CH; ++k) {
+                mv[k] = -1e30f;
+                lv[k] = 0.f;
+                av[k] = make_float2(0.f, 0.f);
+                if (sp0 + k < ns) {
+                    const float *pp = prow + (long long)(sp0 + k) * sstr;
+                    mv[k] = __ldcg(pp + m.d);
+                    lv[k] = __ldcg(pp + m.d + 1);
+                    av[k] = __ldcg(reinterpret_cast<const float2 *>(pp + 2 * dp));
+                }
+            }
+            float cm = M;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) acc += w[sp + k] * v[k];
+            for (int k = 0; k < CH; ++k) cm = fmaxf(cm, mv[k]);
+            const float sc = exp2f(M - cm);
+            lsum *= sc;
+            acc.x *= sc;
+            acc.y *= sc;
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                const float w = exp2f(mv[k] - cm);
+                lsum += w * lv[k];
+                acc.x += w * av[k].x;
+                acc.y += w * av[k].y;
+            }
+            M = cm;
         }
-        for (; sp < ns; ++sp) acc += w[sp] * __ldcg(pp + (long long)sp * MK_MAXROWS * D2);
-        int row = r0 + rr, t = row / G, h = u.g * G + (row - t * G);
-        __stcg(m.o_buf + (long long)t * m.Hq * m.d + h * m.d + dd, acc);
+        const float il = 1.f / lsum;
+        const int row = r0 + rr, t = row / G, h = u.g * G + (row - t * G);
+        __stcg(reinterpret_cast<float2 *>(m.o_buf + (long long)t * m.Hq * m.d + h * m.d + 2 * dp),
+               make_float2(acc.x * il, acc.y * il));
     }
     mark(c, ST_ATT * 16 + 3);
     return ci;
@@ -2046,8 +2059,6 @@ __device__ __noinline__ void consumer() {
             grid_arrive(c);
             ci = cons_gemv(ST_SHA, &(L), rt, ci);
             if (!grid_wait(c, 5)) return;
-            compute_inv_rms(c, 1);
-            bar_consumers();
             mark(c, ST_EXPA * 16 + 3);
             route_layer(&L, rt);
             if (c.tid == 0) mbar_arrive(c.route);
