@@ -351,6 +351,9 @@ def stage_breakdown(mk, st, cfg, one, stream, dev):
     one()
     stream.synchronize()
     mk.mk_set_stage_trace(st, None, 0, None)
+    if os.environ.get("MK_TRACE_DUMP"):
+        import numpy as np
+        np.savez_compressed(os.environ["MK_TRACE_DUMP"], barriers=buf.cpu().numpy(), events=ev.cpu().numpy())
     t = buf.cpu().numpy().astype("float64")
     arr, rel = t[:, :, 0], t[:, :, 1]
     names = ["init"] + [STAGES[i % 6] for i in range(6 * cfg.n_layers)] + ["lm_head", "logits_argmax"]
@@ -395,6 +398,11 @@ def stage_breakdown(mk, st, cfg, one, stream, dev):
             if eid >= 900:
                 cyc[eid].append(val)
     names = {0: "wait", 1: "compute", 2: "other"}
+    for eid in sorted(cyc):
+        if eid >= 1990:
+            v = cyc[eid]
+            sys.stderr.write("  probe %d mean %10.1f\n" % (eid, sum(v) / len(v)))
+    cyc = {k: v for k, v in cyc.items() if k < 1990}
     for eid in sorted(cyc):
         v = cyc[eid]
         if eid < 950:

@@ -1125,7 +1125,7 @@ __device__ __forceinline__ void tile_f32(const Ctx &c, int K, int slot, int kc, 
 }
 
 // h_e = silu(a/rms) * (b/rms) fragments of one expert (or the shared one)
-__device__ __forceinline__ float silu_mul(float a, float b) { return a / (1.f + expf(-a)) * b; }
+__device__ __forceinline__ float silu_mul(float a, float b) { return __fdividef(a, 1.f + __expf(-a)) * b; }
 
 // expert intermediate h = silu(a/rms) * (b/rms) of one routed expert (or the
 // shared one) as f16 fragments; eight blocks of loads are issued at once
