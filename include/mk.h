@@ -169,6 +169,23 @@ mk_status mk_decode_step(mk_state *st, const int32_t *draft_tokens, int T,
                          float *out_logits, int32_t *out_accepted, int32_t *out_argmax,
                          void *stream);
 
+/* One verify step for each of n_streams independent streams (the concurrency
+ * workload): stream s has its own block of T tokens, positions ctx_s .. ctx_s+T-1
+ * and page-table row s of kv.
+ *   draft_tokens  dev int32 [n_streams][T]
+ *   positions     dev int32 [n_streams][T]
+ *   out_logits    dev float32 [n_streams][T][vocab]
+ *   out_accepted  dev int32 [n_streams]
+ *   out_argmax    dev int32 [n_streams][T] or NULL
+ * Each stream's results are bit for bit those of mk_decode_step on that stream
+ * alone.  This build runs the streams one after another on `stream` (one launch
+ * per stream, each streaming the weights once); each counts as one step in
+ * mk_get_stats.  Requires vocab > 0, 1 <= T <= max_T, n_streams >= 1 and a page
+ * table with at least n_streams rows. */
+mk_status mk_decode_batch(mk_state *st, int n_streams, const int32_t *draft_tokens, int T,
+                          const int32_t *positions, const mk_kv_cache *kv, float *out_logits,
+                          int32_t *out_accepted, int32_t *out_argmax, void *stream);
+
 /* The same step through HOST buffers: copies the tokens and positions in, runs
  * the step, copies the results out and synchronizes the stream.  out_logits and
  * out_argmax may be NULL.  Returns the device status of the step. */
@@ -237,6 +254,13 @@ mk_status mk_set_routing_trace(mk_state *st, int32_t *trace);
  * weight tile arrived, 2 last tile reduced, 3 routing started (attention:
  * 0 queries ready, 1 pages done, 2 group barrier passed, 3 merge done). */
 mk_status mk_set_stage_trace(mk_state *st, uint64_t *times, int capacity, uint64_t *events);
+
+/* Test hook for the failure path: on every later launch, CTA 0 does not arrive
+ * at grid barrier `barrier` (1-based, in launch order; 0 turns the hook off).
+ * The other CTAs' waits then run out after timeout_ms, the launch ends with
+ * MK_ERR_TIMEOUT in the device status and every CTA returns; nothing traps or
+ * hangs.  mk_reset (with the hook off) restores a working state. */
+mk_status mk_debug_skip_barrier(mk_state *st, int barrier);
 
 /* Synchronize the last stream used and return the device status of the last
  * step (MK_OK, MK_ERR_TIMEOUT or MK_ERR_BAD_INPUT). */

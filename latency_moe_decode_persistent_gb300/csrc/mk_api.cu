@@ -37,6 +37,7 @@ struct mk_state {
     unsigned long long *stage_trace = nullptr;
     int stage_cap = 0;
     unsigned long long *marks = nullptr;
+    int skip_barrier = 0;
     bool launched = false;
     char err[512] = {0};
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -385,6 +386,7 @@ static mk_status launch(mk_state *st, Params &p, void *stream) {
     p.stage_trace = st->stage_trace;
     p.stage_cap = st->stage_cap;
     p.marks = st->marks;
+    p.skip_barrier = st->skip_barrier;
     p.kvmaps = st->d_kvmaps;
     p.kpool = st->d_kpool;
     p.vpool = st->d_vpool;
@@ -419,6 +421,26 @@ mk_status mk_decode_step(mk_state *st, const int32_t *draft_tokens, int T, const
     p.out_argmax = out_argmax;
     p.trace = st->trace;
     return launch(st, p, stream);
+}
+
+mk_status mk_decode_batch(mk_state *st, int n_streams, const int32_t *draft_tokens, int T,
+                          const int32_t *positions, const mk_kv_cache *kv, float *out_logits,
+                          int32_t *out_accepted, int32_t *out_argmax, void *stream) {
+    if (!st) return MK_ERR_INVALID;
+    if (n_streams < 1) return fail(st, MK_ERR_INVALID, "n_streams = %d", n_streams);
+    if (!kv || !kv->page_table) return fail(st, MK_ERR_INVALID, "bad kv cache descriptor");
+    const long long V = st->desc.vocab, P = st->desc.max_pages_per_stream;
+    for (int s = 0; s < n_streams; ++s) {
+        mk_kv_cache row = *kv;
+        row.page_table = kv->page_table + (long long)s * P;
+        mk_status r = mk_decode_step(st, draft_tokens ? draft_tokens + (long long)s * T : nullptr, T,
+                                     positions ? positions + (long long)s * T : nullptr, &row,
+                                     out_logits ? out_logits + (long long)s * T * V : nullptr,
+                                     out_accepted ? out_accepted + s : nullptr,
+                                     out_argmax ? out_argmax + (long long)s * T : nullptr, stream);
+        if (r != MK_OK) return r;
+    }
+    return MK_OK;
 }
 
 mk_status mk_decode_step_host(mk_state *st, const int32_t *h_tokens, int T, const int32_t *h_positions,
@@ -475,6 +497,12 @@ mk_status mk_set_stage_trace(mk_state *st, uint64_t *times, int capacity, uint64
     st->stage_trace = reinterpret_cast<unsigned long long *>(times);
     st->stage_cap = times ? capacity : 0;
     st->marks = reinterpret_cast<unsigned long long *>(events);
+    return MK_OK;
+}
+
+mk_status mk_debug_skip_barrier(mk_state *st, int barrier) {
+    if (!st || barrier < 0) return MK_ERR_INVALID;
+    st->skip_barrier = barrier;
     return MK_OK;
 }
 

@@ -121,6 +121,7 @@ struct Params {
     unsigned long long *stage_trace;   // [G][cap][2] barrier arrive/release times or null
     int stage_cap;
     unsigned long long *marks;         // [G][MK_MARKS][2] (event id, time) or null
+    int skip_barrier;                  // test hook: CTA 0 skips this grid-barrier arrival (0: none)
 };
 
 // one kernel per model class (mk_kernel.cu compiled twice): _f32 for all-fp32

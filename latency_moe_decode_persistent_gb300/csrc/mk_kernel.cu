@@ -440,7 +440,9 @@ __device__ void grid_arrive(const Ctx &c) {
         if (p.stage_trace && nbar <= p.stage_cap)
             p.stage_trace[((long long)c.cta * p.stage_cap + nbar - 1) * 2] = gtimer();
         __threadfence();
-        atomicAdd(&c.ctrl->bar_count, 1ull);
+        // test hook (mk_debug_skip_barrier): CTA 0 withholds one arrival so that
+        // every other CTA's bounded wait runs out
+        if (!(p.skip_barrier == nbar && c.cta == 0)) atomicAdd(&c.ctrl->bar_count, 1ull);
     }
 }
 __device__ bool grid_wait(const Ctx &c, int where) {
@@ -835,9 +837,13 @@ __device__ __noinline__ void producer() {
         ok = prod_gemv(c, ps, ST_EXPA, L, rt) && prod_gemv(c, ps, ST_EXPB, L, rt);
     }
     if (ok && p.mode == 0) ok = prod_gemv(c, ps, ST_LM, c.misc->L[0], &c.rt[0]);
-    // after a failure, the last copy this lane issued must land before the CTA exits
-    // (earlier copies into the same slot completed before it was re-armed)
-    if (!ok && ps.last >= 0) mbar_wait_drain(&c.full[ps.last % MK_RING], (ps.last / MK_RING) & 1, c);
+    // after a failure every copy this lane may still have in flight must land
+    // before the CTA exits: those are the last MK_RING armed ring positions (a
+    // slot is re-armed only after its previous copy completed and was consumed;
+    // a position whose copy already landed passes its wait at once)
+    if (!ok && ps.last >= 0)
+        for (int pos = max(0, ps.last - (MK_RING - 1)); pos <= ps.last; ++pos)
+            mbar_wait_drain(&c.full[pos % MK_RING], (pos / MK_RING) & 1, c);
 }
 
 // ------------------------------------------------------------------ activations

@@ -21,8 +21,8 @@ MK_DT_F32, MK_DT_BF16, MK_DT_FP8E4M3_B128 = 0, 1, 2
 MK_DESC_VERSION = 1
 
 #: every symbol include/mk.h declares
-EXPORTS = ["mk_create", "mk_decode_step", "mk_decode_step_host", "mk_layer_forward",
-           "mk_get_status", "mk_get_stats", "mk_set_routing_trace", "mk_set_stage_trace", "mk_reset", "mk_layer_forward_noalloc", "mk_destroy", "mk_status_string",
+EXPORTS = ["mk_create", "mk_decode_step", "mk_decode_batch", "mk_decode_step_host", "mk_layer_forward",
+           "mk_get_status", "mk_get_stats", "mk_debug_skip_barrier", "mk_set_routing_trace", "mk_set_stage_trace", "mk_reset", "mk_layer_forward_noalloc", "mk_destroy", "mk_status_string",
            "mk_last_error"]
 
 _vp = ctypes.c_void_p
@@ -85,6 +85,9 @@ def lib() -> ctypes.CDLL:
     L.mk_decode_step.argtypes = [_vp, _vp, ctypes.c_int, _vp, ctypes.POINTER(mk_kv_cache), _vp,
                                  _vp, _vp, _vp]
     L.mk_decode_step.restype = S
+    L.mk_decode_batch.argtypes = [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp,
+                                  ctypes.POINTER(mk_kv_cache), _vp, _vp, _vp, _vp]
+    L.mk_decode_batch.restype = S
     L.mk_decode_step_host.argtypes = L.mk_decode_step.argtypes
     L.mk_decode_step_host.restype = S
     L.mk_layer_forward.argtypes = [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp,
@@ -99,6 +102,8 @@ def lib() -> ctypes.CDLL:
     L.mk_set_routing_trace.restype = S
     L.mk_set_stage_trace.argtypes = [_vp, _vp, ctypes.c_int, _vp]
     L.mk_set_stage_trace.restype = S
+    L.mk_debug_skip_barrier.argtypes = [_vp, ctypes.c_int]
+    L.mk_debug_skip_barrier.restype = S
     L.mk_get_status.argtypes = [_vp]
     L.mk_get_status.restype = S
     L.mk_get_stats.argtypes = [_vp, ctypes.POINTER(mk_stats)]
@@ -156,6 +161,18 @@ def mk_decode_step(st, draft_tokens, T, positions, kv: mk_kv_cache, out_logits, 
                    out_argmax=None, stream=None, check=True) -> int:
     s = lib().mk_decode_step(st, _ptr(draft_tokens), T, _ptr(positions), ctypes.byref(kv),
                              _ptr(out_logits), _ptr(out_accepted), _ptr(out_argmax), _ptr(stream))
+    return _check(st, s) if check else s
+
+
+def mk_debug_skip_barrier(st, barrier: int) -> int:
+    return lib().mk_debug_skip_barrier(st, barrier)
+
+
+def mk_decode_batch(st, n_streams, draft_tokens, T, positions, kv: mk_kv_cache, out_logits,
+                    out_accepted, out_argmax=None, stream=None, check=True) -> int:
+    s = lib().mk_decode_batch(st, n_streams, _ptr(draft_tokens), T, _ptr(positions),
+                              ctypes.byref(kv), _ptr(out_logits), _ptr(out_accepted),
+                              _ptr(out_argmax), _ptr(stream))
     return _check(st, s) if check else s
 
 

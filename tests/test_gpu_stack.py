@@ -148,3 +148,67 @@ def test_block_verification_is_batch_invariant():
             assert torch.equal(am, am_full[:n])
     finally:
         b.close()
+
+
+def test_decode_batch_matches_single_streams():
+    """mk_decode_batch over two streams with different contexts gives each stream
+    exactly the result of mk_decode_step on that stream alone."""
+    cfg = mini_stack(seed=61)
+    ctxs = [200, 131]
+    b = gc.Built(cfg, ctxs=ctxs)
+    try:
+        S, T, V = len(ctxs), cfg.T, cfg.vocab
+        rng = np.random.default_rng(4)
+        toks = torch.tensor(rng.integers(0, V, (S, T)), dtype=torch.int32, device="cuda")
+        pos = torch.stack([torch.arange(c, c + T, dtype=torch.int32) for c in ctxs]).cuda()
+        logits = torch.empty((S, T, V), dtype=torch.float32, device="cuda")
+        acc = torch.zeros(S, dtype=torch.int32, device="cuda")
+        am = torch.zeros((S, T), dtype=torch.int32, device="cuda")
+        mk.mk_decode_batch(b.st, S, toks, T, pos, b.kvargs.kv, logits, acc, am)
+        assert mk.mk_get_status(b.st) == mk.MK_OK
+        for s in range(S):
+            kv1 = mk.KVArgs(b.kv.k_pools, b.kv.v_pools, b.kv.page_table[s], b.kv.n_pages)
+            lg = torch.empty((T, V), dtype=torch.float32, device="cuda")
+            a1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+            m1 = torch.zeros(T, dtype=torch.int32, device="cuda")
+            mk.mk_decode_step(b.st, toks[s].contiguous(), T, pos[s].contiguous(), kv1.kv, lg, a1, m1)
+            assert mk.mk_get_status(b.st) == mk.MK_OK
+            assert torch.equal(lg, logits[s]) and int(a1) == int(acc[s]) and torch.equal(m1, am[s])
+        # stream 1 against the oracle as well (its own page-table row and context)
+        dims = helpers.oracle_dims(cfg)
+        layers = [helpers.layer_view(b.model, l) for l in range(cfg.n_layers)]
+        kvs = [helpers.kv_view(b.kv, l, stream=1) for l in range(cfg.n_layers)]
+        r = oracle.stack_forward(toks[1].tolist(), helpers.embed_fn(b.model), layers,
+                                 b.model.final_norm.cpu().numpy().astype(np.float64),
+                                 helpers.lm_head_lin(b.model), dims, kvs, ctxs[1])
+        assert helpers.rel_err(logits[1].cpu().numpy(), r["logits"]) < gc.TOL[synth.WDT_FP8]
+    finally:
+        b.close()
+
+
+def test_timeout_is_reported_and_reset_recovers():
+    """Failure path without a GPU fault: CTA 0 withholds one grid-barrier arrival
+    (a test hook), every other CTA's bounded wait runs out after timeout_ms, the
+    step reports MK_ERR_TIMEOUT, later steps refuse to run until mk_reset, and
+    after mk_reset the state computes the same logits as before."""
+    cfg = mini_stack(seed=71)
+    b = gc.Built(cfg, timeout_ms=50)
+    try:
+        toks = [7, 8, 9, 10, 11, 12]
+        ref, acc_ref, _, _ = b.step(toks, trace=False)
+        ref = ref.clone()
+        mk.mk_debug_skip_barrier(b.st, 2)
+        tok = torch.tensor(toks, dtype=torch.int32, device="cuda")
+        logits = torch.empty_like(ref)
+        acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pos = b.positions(len(toks))
+        mk.mk_decode_step(b.st, tok, len(toks), pos, b.kvargs.kv, logits, acc, None)
+        assert mk.mk_get_status(b.st) == mk.MK_ERR_TIMEOUT
+        mk.mk_debug_skip_barrier(b.st, 0)
+        mk.mk_decode_step(b.st, tok, len(toks), pos, b.kvargs.kv, logits, acc, None)
+        assert mk.mk_get_status(b.st) == mk.MK_ERR_TIMEOUT   # sticky until reset
+        assert mk.mk_reset(b.st) == mk.MK_OK
+        again, acc2, _, _ = b.step(toks, trace=False)
+        assert torch.equal(again, ref) and acc2 == acc_ref
+    finally:
+        b.close()
