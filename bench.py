@@ -185,7 +185,12 @@ def run_mk(args):
         import torch.distributed as dist
         dist.init_process_group("gloo")
         pg = dist
-    cfg = synth.stack_config(n_layers=args.layers) if args.layers else synth.stack_config()
+    kw = {}
+    if args.layers:
+        kw["n_layers"] = args.layers
+    if args.T:
+        kw["T"] = args.T
+    cfg = synth.stack_config(**kw)
     t_gen = time.perf_counter()
     model = synth.make_model(cfg, dev)
     kv = synth.make_kv(cfg, dev)
@@ -335,6 +340,80 @@ def run_mk(args):
     mk.mk_destroy(st)
 
 
+def run_streams(args):
+    """Concurrency workload: S independent streams, each a T=6 block at its own
+    context (U[1024, 8192], seed 4) over the 43-layer FP8 stack, verified by
+    mk_decode_batch.  Drafts per stream as in the single-stream workload."""
+    import numpy as np
+    import torch
+    from latency_moe_decode_persistent_gb300 import mk, synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    S = args.streams
+    rng = np.random.default_rng(4)
+    ctxs = [int(c) for c in rng.integers(1024, 8193, S)]
+    cfg = synth.stack_config(seed=4, **({"n_layers": args.layers} if args.layers else {}))
+    model = synth.make_model(cfg, dev)
+    kv = synth.make_kv(cfg, dev, ctxs=ctxs)
+    margs = mk.ModelArgs(model, cfg.T, kv.max_pages)
+    st = mk.mk_create(margs.desc, margs.weights)
+    kva = mk.KVArgs(kv.k_pools, kv.v_pools, kv.page_table, kv.n_pages)
+    T, V = cfg.T, cfg.vocab
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    logits = torch.empty((S, T, V), dtype=torch.float32, device=dev)
+    acc = torch.zeros(S, dtype=torch.int32, device=dev)
+    am = torch.zeros((S, T), dtype=torch.int32, device=dev)
+    pos = torch.stack([torch.arange(c, c + T, dtype=torch.int32) for c in ctxs]).to(dev)
+    toks = []
+    for s in range(S):
+        row = mk.KVArgs(kv.k_pools, kv.v_pools, kv.page_table[s], kv.n_pages)
+
+        def step_prefix(tk, s=s, row=row):
+            n = len(tk)
+            t = torch.tensor(tk, dtype=torch.int32, device=dev)
+            mk.mk_decode_step(st, t, n, pos[s, :n].contiguous(), row.kv, logits[s], acc[s:], am[s], sh)
+            stream.synchronize()
+            return am[s, :n].cpu().tolist()
+        toks.append(make_drafts(step_prefix, V, 2000 + s, T - 1, 0.83, seed=40 + s))
+    tok = torch.tensor(toks, dtype=torch.int32, device=dev)
+
+    def one():
+        mk.mk_decode_batch(st, S, tok, T, pos, kva.kv, logits, acc, am, sh)
+
+    for _ in range(max(args.warmup, 3)):
+        one()
+    stream.synchronize()
+    s0 = mk.mk_get_stats(st)
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for _ in range(args.steps):
+        one()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    if mk.mk_get_status(st) != mk.MK_OK:
+        raise RuntimeError("device status: " + mk.mk_last_error(st))
+    s1 = mk.mk_get_stats(st)
+    ms = g0.elapsed_time(g1) / args.steps
+    n = s1.steps - s0.steps
+    acc_mean = (s1.accepted_sum - s0.accepted_sum) / max(n, 1)
+    distinct = (s1.distinct_experts_sum - s0.distinct_experts_sum) / max(n, 1) / cfg.n_layers
+    per_stream = (acc_mean + 1.0) / (ms / 1e3)
+    print(json.dumps({
+        "metric": "verify-step us and tok/s, %d concurrent streams (43-layer FP8, T=6)" % S,
+        "value": round(per_stream * S, 3), "unit": "tok/s (all streams)", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "per_stream_tok_s": round(per_stream, 3),
+        "tokens_per_stream_step": round(acc_mean + 1.0, 4),
+        "distinct_experts_per_layer_per_stream": round(distinct, 2),
+        "launches_per_step": S, "dtype": "fp8e4m3 weights x f16 activations -> fp32",
+        "data": "synthetic", "config": {"workload": "%d streams x T=6, contexts %s, seed 4; streams run one "
+                                                    "after another (one launch each)" % (S, ctxs)}}), flush=True)
+    mk.mk_destroy(st)
+
+
 STAGES = ["qkv", "attention", "o_proj", "router+shared_gate_up", "routed_gate_up", "routed_down"]
 
 
@@ -476,9 +555,15 @@ def main():
     ap.add_argument("--ref-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-trace", action="store_true", help="print an in-kernel stage breakdown to stderr")
+    ap.add_argument("--T", type=int, default=0, help="verify block size (T sweep; default 6)")
+    ap.add_argument("--streams", type=int, default=0,
+                    help="concurrency workload: S streams of T=6 tokens, contexts U[1024, 8192], seed 4 "
+                         "(mk_decode_batch); prints its own line")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.streams:
+        run_streams(args)
     else:
         run_mk(args)
 
