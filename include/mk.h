@@ -71,9 +71,12 @@ enum {
 #define MK_DESC_VERSION 1
 
 /* Model description.  Limits of this build: T <= 8; hidden, expert_inter and
- * n_q_heads*head_dim multiples of 128 and <= 4096; head_dim 64 or 128;
- * page_size 64; (n_q_heads/n_kv_heads)*T <= 64; n_experts <= 512; top_k <= 8;
- * n_shared 0 or 1; F32 weights only with hidden <= 2048 and an all-F32 model. */
+ * n_q_heads*head_dim multiples of 128 and <= 4096; page_size 64;
+ * (n_q_heads/n_kv_heads)*T <= 64; n_experts a multiple of 4 and <= 512;
+ * top_k <= 8; n_shared 0 or 1.  bf16 / FP8 weights need a bf16 KV cache and
+ * head_dim 128.  F32 weights need an F32 router, head_dim 64,
+ * (n_q_heads/n_kv_heads)*T <= 16 and hidden, n_q_heads*head_dim,
+ * expert_inter <= 2048. */
 typedef struct {
     int version;              /* MK_DESC_VERSION                                      */
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim;

@@ -13,7 +13,6 @@
 #define MK_RING 4                        // shared-memory ring slots
 #define MK_SLOT 32768                    // bytes per slot: one 256-row x 128-byte TMA box
 #define MK_PLANES 1                      // producer lanes issuing copies side by side
-#define MK_PF 8                          // L2 prefetch distance in tiles (multiple of MK_PLANES)
 #define MK_MAXT 8                        // tokens per verify block (one N=8 MMA tile)
 #define MK_MAXKB 32                      // 128-column blocks of the widest GEMV input (4096)
 #define MK_MAXE 512                      // routed experts

@@ -10,21 +10,21 @@
 // persistent CTA per SM as the megakernel plugin does ("DeepSeek-V4.1-Flash breaks
 // 1,000 tokens per second for one user", section "What NVIDIA shipped").
 //
-// Structure of a CTA (288 threads):
-//   warp 8      producer: walks the CTA's static chunk schedule for the whole
-//               step and streams weight tiles / KV pages into an 8-slot shared
-//               memory ring with TMA (cp.async.bulk.tensor, 128-byte swizzle)
-//               plus 1-D bulk copies of FP8 block scales.  It runs ahead across
-//               grid barriers; it only stops for a free slot, and for the router
-//               result before the routed-expert tiles of a layer.
-//   warps 0..7  consumers: every 16 KB tile is 128 rows x 128 bytes of one
-//               matrix; warp w reduces rows 16w..16w+15 against the T <= 8
-//               activations with mma.sync m16n8k16 (tokens are the N=8 side;
-//               FP8 codes are widened to f16 in registers, scales applied per
-//               1x128 block), accumulating across consecutive tiles of a row
-//               group, then adds its partial into a global fixed-point (2^-32)
-//               int64 accumulator.  Integer adds make every cross-CTA reduction
-//               order-independent, so the step is bitwise deterministic.
+// Structure of a CTA (288 threads, one CTA per SM):
+//   warp 8      producer: walks the CTA's static tile schedule for the whole
+//               step and streams weight tiles (256 rows x 128 bytes, one TMA box
+//               with the 128-byte swizzle) and KV pages into a 4-slot shared
+//               memory ring with cp.async.bulk.tensor, plus 1-D bulk copies of
+//               the FP8 block scales, all with an L2 evict-first hint.  It runs
+//               ahead across grid barriers; it only stops for a free slot, and
+//               for the router result before the routed-expert tiles of a layer.
+//   warps 0..7  consumers: warp w reduces rows 32w..32w+31 of each tile against
+//               the T <= 8 activations with mma.sync m16n8k16 (tokens are the
+//               N = 8 side; FP8 codes are widened to f16 in registers and the
+//               1x128 scales applied per block), accumulating across consecutive
+//               tiles of an item, then adds its partial into a global fixed-point
+//               (2^-32) int64 accumulator.  Integer adds make every cross-CTA
+//               reduction order-independent, so the step is bitwise deterministic.
 // RMSNorm is folded: GEMVs consume gamma*x and the consumer of their result
 // divides by rms(x), whose sum of squares is computed by 32 CTAs in parallel.
 // Grid barriers (monotonic counter, acquire/release) separate the stages; every
@@ -125,18 +125,6 @@ __device__ __forceinline__ void bulk_g2s_h(void *dst, const void *src, uint32_t 
         "l"(src), "r"(bytes), "r"(sa(bar)), "l"(pol)
         : "memory");
 }
-__device__ __forceinline__ void tma_prefetch2d(const CUtensorMap *map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
-                 : "memory");
-}
-__device__ __forceinline__ void tma_prefetch3d(const CUtensorMap *map, int x, int y, int z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x),
-                 "r"(y), "r"(z)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_prefetch(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
                                          uint64_t *bar) {
     asm volatile(
@@ -182,14 +170,6 @@ __device__ __forceinline__ void mma_bf16(float *c, uint32_t a0, uint32_t a1, uin
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// two FP8 E4M3 codes (low byte first) -> f16x2 (low half first)
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t v16) {
-    uint32_t r;
-    asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n"
-        : "=r"(r)
-        : "r"(v16));
-    return r;
 }
 // four FP8 E4M3 codes (byte 0 first) -> two f16x2 words (bytes 0,1 and 2,3)
 __device__ __forceinline__ void e4m3x4_f16(uint32_t v, uint32_t &lo, uint32_t &hi) {
@@ -465,11 +445,6 @@ __device__ bool grid_sync(const Ctx &c, int where) {
 }
 
 // ------------------------------------------------------------------ schedules
-struct Item {
-    const DMat *m;
-    int e, rg, kc, mat, ex;
-};
-
 __device__ __forceinline__ void split_range(int total, int parts, int part, int &b, int &e) {
     b = (int)((long long)total * part / parts);
     e = (int)((long long)total * (part + 1) / parts);
@@ -488,53 +463,6 @@ __device__ int stage_total(const DModel &m, int st, const DLayer &L, const Route
     return 0;
 }
 
-__device__ Item stage_item(const DModel &m, int st, const DLayer &L, const RouteSm *rt, int idx) {
-    Item it;
-    it.e = 0;
-    it.mat = 0;
-    it.ex = 0;
-    const DMat *d;
-    int r = idx;
-    switch (st) {
-        case ST_QKV: d = &L.qkv; break;
-        case ST_O: d = &L.o; break;
-        case ST_ROUTER: d = &L.router; break;
-        case ST_LM: d = &m.lm; break;
-        case ST_SHA: {
-            int per = L.s1.n_rg * L.s1.n_kc;
-            it.mat = r / per;
-            r -= it.mat * per;
-            d = it.mat ? &L.s3 : &L.s1;
-            break;
-        }
-        case ST_EXPA: {
-            int per1 = L.w1.n_rg * L.w1.n_kc;
-            it.ex = r / (2 * per1);
-            r -= it.ex * 2 * per1;
-            it.mat = r / per1;
-            r -= it.mat * per1;
-            d = it.mat ? &L.w3 : &L.w1;
-            it.e = rt->dlist[it.ex];
-            break;
-        }
-        default: {  // ST_EXPB
-            int per = L.w2.n_rg * L.w2.n_kc;
-            it.ex = r / per;
-            r -= it.ex * per;
-            if (it.ex < rt->nd) {
-                d = &L.w2;
-                it.e = rt->dlist[it.ex];
-            } else {
-                d = &L.s2;
-            }
-            break;
-        }
-    }
-    it.m = d;
-    it.rg = r / d->n_kc;
-    it.kc = r - it.rg * d->n_kc;
-    return it;
-}
 
 // attention split of a unit (one kv head, a run of pages)
 struct AttUnit {
@@ -719,16 +647,6 @@ __device__ __forceinline__ bool prod_take(const Ctx &c, Prod &ps, uint32_t pos, 
     return true;
 }
 
-// L2 prefetch of the tile at the iterator's position (weights and FP8 scales)
-__device__ __forceinline__ void prefetch_tile(const StageIter &it) {
-    const MatR &d = it.cur();
-    const int e = it.expert();
-    const int x = it.kc * d.xstep, y = it.rg * 256;
-    if (d.is3d) tma_prefetch3d(d.tmap, x, y, e);
-    else tma_prefetch2d(d.tmap, x, y);
-    if (d.dtype == MK_DT_FP8E4M3_B128)
-        bulk_prefetch(d.scale + (long long)e * d.sest + (long long)it.kc * d.rows + y, min(256, d.rows - y) * 4);
-}
 
 __device__ __forceinline__ bool prod_gemv_impl(const Ctx &c, Prod &ps, int st, const DLayer &L,
                                                const RouteSm *rt) {
