@@ -174,6 +174,24 @@ def make_drafts(step_fn, vocab, d0, k, p, seed):
     return toks
 
 
+def reduce_over_ranks(mean_ms, tok_per_step, e2e_s, e2e_tok, distributed):
+    """Whole-job figures of the replicas: the slowest rank's step time, and tokens
+    summed over ranks divided by that time (device-timed and end to end).  Rank
+    timings meet through the process group's CPU backend; no data-path
+    collective is involved.  Returns (slowest ms, tok/s, e2e tok/s)."""
+    if not distributed:
+        return mean_ms, tok_per_step / (mean_ms / 1e3), e2e_tok
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([mean_ms, tok_per_step, e2e_s, e2e_tok], dtype=torch.float64)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    sm = t.clone()
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    slow_ms = float(mx[0])
+    return slow_ms, float(sm[1]) / (slow_ms / 1e3), float(sm[1]) / float(mx[2])
+
+
 def run_mk(args):
     import torch
     from latency_moe_decode_persistent_gb300 import mk, synth
@@ -277,22 +295,9 @@ def run_mk(args):
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     e2e_tok = (int(h_acc.item()) + 1) / e2e_s
 
-    # reduce over ranks: slowest time, summed tokens
     mean_ms = total_ms / args.steps
-    if pg:
-        import torch.distributed as dist
-        t = torch.tensor([mean_ms, tok_per_step, e2e_s, e2e_tok], dtype=torch.float64)
-        mx = t.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        sm = t.clone()
-        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
-        slow_ms = float(mx[0])
-        value = float(sm[1]) / (slow_ms / 1e3)
-        e2e_value = float(sm[1]) / float(mx[2])
-    else:
-        slow_ms = mean_ms
-        value = tok_per_step / (mean_ms / 1e3)
-        e2e_value = e2e_tok
+    slow_ms, value, e2e_value = reduce_over_ranks(mean_ms, tok_per_step, e2e_s, e2e_tok,
+                                                  pg is not None)
     if rank != 0:
         mk.mk_destroy(st)
         return
