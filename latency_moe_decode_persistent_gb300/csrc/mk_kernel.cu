@@ -309,18 +309,23 @@ __device__ __forceinline__ Ctx make_ctx() {
     return c;
 }
 
-// intra-stage trace event (thread 0 of the consumers, only when tracing)
-__device__ __forceinline__ void mark(const Ctx &c, int id) {
+// intra-stage trace event (thread 0 of the consumers, only when tracing).
+// Helpers that run at many call sites but rarely or off the hot loop are kept
+// out of line: most of the step's code runs once per layer, so every inlined
+// copy is code the instruction cache fetches again each layer.
+__device__ __noinline__ void mark_slow(int id) {
+    const Ctx c = make_ctx();
     const Params &p = *c.p;
-    if (p.marks && c.tid == 0) {
-        const int k = c.misc->nmark;
-        if (k < MK_MARKS - 80) {
-            unsigned long long *e = p.marks + ((long long)c.cta * MK_MARKS + k) * 2;
-            e[0] = (unsigned long long)id;
-            e[1] = gtimer();
-        }
-        c.misc->nmark = k + 1;
+    const int k = c.misc->nmark;
+    if (k < MK_MARKS - 80) {
+        unsigned long long *e = p.marks + ((long long)c.cta * MK_MARKS + k) * 2;
+        e[0] = (unsigned long long)id;
+        e[1] = gtimer();
     }
+    c.misc->nmark = k + 1;
+}
+__device__ __forceinline__ void mark(const Ctx &c, int id) {
+    if (c.prof && c.tid == 0) mark_slow(id);
 }
 
 // trace value written at a fixed event slot (cycle counts of a loop)
@@ -348,9 +353,9 @@ __device__ void raise_err(const Ctx &c, int code, int where) {
     if (atomicCAS(&c.ctrl->status, 0, code) == 0) atomicExch(&c.ctrl->where, where);
     atomicExch(&c.ctrl->abort, 1);
 }
-// bounded wait on an mbarrier phase
-__device__ bool mbar_wait(uint64_t *b, uint32_t parity, const Ctx &c, int where) {
-    if (mbar_try(b, parity)) return true;
+// bounded wait on an mbarrier phase: first try inline, the rest out of line
+__device__ __noinline__ bool mbar_wait_slow(uint64_t *b, uint32_t parity, int where) {
+    const Ctx c = make_ctx();
     uint64_t t0 = gtimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(b, parity)) return true;
@@ -362,6 +367,10 @@ __device__ bool mbar_wait(uint64_t *b, uint32_t parity, const Ctx &c, int where)
             }
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, const Ctx &c, int where) {
+    (void)c;
+    return mbar_try(b, parity) || mbar_wait_slow(b, parity, where);
 }
 // bounded wait that ignores the abort flag (drain of copies in flight)
 __device__ void mbar_wait_drain(uint64_t *b, uint32_t parity, const Ctx &c) {
@@ -412,7 +421,8 @@ __device__ bool spin_ge_s32(int *a, int target, const Ctx &c, int where) {
 }
 
 // grid-wide barrier among the consumer warps of all CTAs; split into arrive/wait
-__device__ void grid_arrive(const Ctx &c) {
+__device__ __noinline__ void grid_arrive_nc() {
+    const Ctx c = make_ctx();
     bar_consumers();
     if (c.tid == 0) {
         const int nbar = ++c.misc->nbar;
@@ -425,7 +435,8 @@ __device__ void grid_arrive(const Ctx &c) {
         if (!(p.skip_barrier == nbar && c.cta == 0)) atomicAdd(&c.ctrl->bar_count, 1ull);
     }
 }
-__device__ bool grid_wait(const Ctx &c, int where) {
+__device__ __noinline__ bool grid_wait_nc(int where) {
+    const Ctx c = make_ctx();
     if (c.tid == 0) {
         const int nbar = c.misc->nbar;
         bool ok = !aborted_global(c);
@@ -439,7 +450,15 @@ __device__ bool grid_wait(const Ctx &c, int where) {
     bar_consumers();
     return c.misc->gs_ok != 0;
 }
-__device__ bool grid_sync(const Ctx &c, int where) {
+__device__ __forceinline__ void grid_arrive(const Ctx &c) {
+    (void)c;
+    grid_arrive_nc();
+}
+__device__ __forceinline__ bool grid_wait(const Ctx &c, int where) {
+    (void)c;
+    return grid_wait_nc(where);
+}
+__device__ __forceinline__ bool grid_sync(const Ctx &c, int where) {
     grid_arrive(c);
     return grid_wait(c, where);
 }
@@ -1184,12 +1203,18 @@ __device__ __noinline__ uint32_t cons_gemv(int st, const DLayer *Lp, const Route
 }
 
 // ------------------------------------------------------------------ small helpers
-__device__ void zero_slice(const Ctx &c, long long *p, long long n) {
+__device__ __noinline__ void zero_slice_nc(long long *p, long long n) {
+    const Ctx c = make_ctx();
     long long b = n * c.cta / c.G, e = n * (c.cta + 1) / c.G;
     for (long long i = b + c.tid; i < e; i += MK_NCWARPS * 32) __stcg(p + i, 0ll);
 }
+__device__ __forceinline__ void zero_slice(const Ctx &c, long long *p, long long n) {
+    (void)c;
+    zero_slice_nc(p, n);
+}
 // sum of squares of 128-column block `kb` of the residual for every token
-__device__ void ssq_block(const Ctx &c, int which) {
+__device__ __noinline__ void ssq_block_nc(int which) {
+    const Ctx c = make_ctx();
     const DModel &m = *c.m;
     int kb = c.cta;
     if (kb >= m.H / 128) return;
@@ -1204,7 +1229,12 @@ __device__ void ssq_block(const Ctx &c, int which) {
     for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
     if (c.lane == 0) __stcg(m.ssq + (which * MK_MAXKB + kb) * MK_MAXT + t, s);
 }
-__device__ void compute_inv_rms(const Ctx &c, int which) {
+__device__ __forceinline__ void ssq_block(const Ctx &c, int which) {
+    (void)c;
+    ssq_block_nc(which);
+}
+__device__ __noinline__ void compute_inv_rms_nc(int which) {
+    const Ctx c = make_ctx();
     const DModel &m = *c.m;
     if (c.warp < c.T) {
         const int t = c.warp;
@@ -1213,6 +1243,10 @@ __device__ void compute_inv_rms(const Ctx &c, int which) {
         for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         if (c.lane == 0) c.misc->inv_rms[which][t] = rsqrtf(v / (float)m.H + m.eps);
     }
+}
+__device__ __forceinline__ void compute_inv_rms(const Ctx &c, int which) {
+    (void)c;
+    compute_inv_rms_nc(which);
 }
 
 // ------------------------------------------------------------------ routing
@@ -1895,10 +1929,15 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
 
 // ------------------------------------------------------------------ consumer
 // copy one layer's descriptors into shared memory (consumer threads)
-__device__ __forceinline__ void copy_layer(const Ctx &c, DLayer *dst, const DLayer *src) {
+__device__ __noinline__ void copy_layer_nc(DLayer *dst, const DLayer *src) {
+    const Ctx c = make_ctx();
     const int nw = (int)(sizeof(DLayer) / 4);
     for (int i = c.tid; i < nw; i += MK_NCWARPS * 32)
         reinterpret_cast<uint32_t *>(dst)[i] = __ldg(reinterpret_cast<const uint32_t *>(src) + i);
+}
+__device__ __forceinline__ void copy_layer(const Ctx &c, DLayer *dst, const DLayer *src) {
+    (void)c;
+    copy_layer_nc(dst, src);
 }
 
 __device__ __noinline__ void consumer() {
