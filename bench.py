@@ -62,7 +62,7 @@ def kernel_source_hash():
 def ncu_traffic():
     """Per-launch DRAM bytes of the step kernel from the committed ncu summary,
     only if it was captured on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "mk_step_kernel_traffic.json")
+    p = os.path.join(ROOT, "profiles", "mk_step_kernel_traffic.txt")
     try:
         d = json.load(open(p))
     except Exception:
@@ -73,7 +73,7 @@ def ncu_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -83,7 +83,7 @@ class ClockSampler:
         self.p = None
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.Q,
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.p = None
