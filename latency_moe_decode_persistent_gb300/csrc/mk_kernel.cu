@@ -1876,18 +1876,22 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     split_range(R, c.nsplit, u.s, r0, r1);
     const int nr = r1 - r0, ns = c.nsplit;
     const float *pbase = m.att_part + (long long)(u.g * MK_MAXSPLIT) * MK_MAXROWS * D2;
-    // log-sum-exp merge of my rows: thread (row, column pair) reads every
-    // split's (m, l) and partial output in chunks of 16 splits, all loads of a
-    // chunk in flight at once, and folds them with the running maximum
+    // log-sum-exp merge of my rows: two adjacent lanes share a (row, column
+    // pair) and take half of the splits each, so that one batch of loads in
+    // flight covers up to 2 * 19 splits; each lane folds its half with the
+    // running maximum, then the two halves are folded by one shuffle
     const int hp = m.d / 2;
-    for (int item = c.tid; item < nr * hp; item += MK_NCWARPS * 32) {
-        const int rr = item / hp, dp = item - rr * hp;
+    const long long sstr = (long long)MK_MAXROWS * D2;
+    for (int item = c.tid; item < nr * hp * 2; item += MK_NCWARPS * 32) {  // warp-uniform bound
+        const int half = item & 1, grp = item >> 1;
+        const int rr = grp / hp, dp = grp - rr * hp;
         const float *prow = pbase + (long long)(r0 + rr) * D2;
-        const long long sstr = (long long)MK_MAXROWS * D2;
+        int s0, s1;
+        split_range(ns, 2, half, s0, s1);
         float M = -1e30f, lsum = 0.f;
         float2 acc = make_float2(0.f, 0.f);
-        constexpr int CH = 16;
-        for (int sp0 = 0; sp0 < ns; sp0 += CH) {
+        constexpr int CH = 19;
+        for (int sp0 = s0; sp0 < s1; sp0 += CH) {
             float mv[CH], lv[CH];
             float2 av[CH];
 #pragma unroll
@@ -1895,7 +1899,7 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
                 mv[k] = -1e30f;
                 lv[k] = 0.f;
                 av[k] = make_float2(0.f, 0.f);
-                if (sp0 + k < ns) {
+                if (sp0 + k < s1) {
                     const float *pp = prow + (long long)(sp0 + k) * sstr;
                     mv[k] = __ldcg(pp + m.d);
                     lv[k] = __ldcg(pp + m.d + 1);
@@ -1918,10 +1922,15 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
             }
             M = cm;
         }
-        const float il = 1.f / lsum;
-        const int row = r0 + rr, t = row / G, h = u.g * G + (row - t * G);
-        __stcg(reinterpret_cast<float2 *>(m.o_buf + (long long)t * m.Hq * m.d + h * m.d + 2 * dp),
-               make_float2(acc.x * il, acc.y * il));
+        const float Mo = __shfl_xor_sync(0xffffffffu, M, 1), lo = __shfl_xor_sync(0xffffffffu, lsum, 1);
+        const float ox = __shfl_xor_sync(0xffffffffu, acc.x, 1), oy = __shfl_xor_sync(0xffffffffu, acc.y, 1);
+        if (half == 0) {
+            const float Mn = fmaxf(M, Mo), a = exp2f(M - Mn), b = exp2f(Mo - Mn);
+            const float il = 1.f / (lsum * a + lo * b);
+            const int row = r0 + rr, t = row / G, h = u.g * G + (row - t * G);
+            __stcg(reinterpret_cast<float2 *>(m.o_buf + (long long)t * m.Hq * m.d + h * m.d + 2 * dp),
+                   make_float2((acc.x * a + ox * b) * il, (acc.y * a + oy * b) * il));
+        }
     }
     mark(c, ST_ATT * 16 + 3);
     return ci;
