@@ -578,6 +578,17 @@ __device__ uint32_t chunk_kb_mask(const Ctx &c, int cols) {
     return msk & all;
 }
 
+// blocks whose sum-of-squares partial this CTA stores in the chunk-major
+// stages: the first CTA of each chunk takes that chunk's blocks (CTA 0 takes
+// every block when the input is not cut into chunks)
+__device__ uint32_t ssq_owner_mask(const Ctx &c, int cols) {
+    const uint32_t all = 0xffffffffu >> (32 - cols / 128);
+    if (cols % 1024) return c.cta == 0 ? all : 0u;
+    const int nch = cols / 1024, c0 = nch * c.cta / c.G;
+    if (c.cta > 0 && nch * (c.cta - 1) / c.G == c0) return 0u;
+    return (0xffu << (8 * c0)) & all;
+}
+
 __device__ void stage_iter(StageIter &it, const Ctx &c, int st, const DLayer &L, const RouteSm *rt) {
     const DModel &m = *c.m;
     it.st = st;
@@ -832,7 +843,10 @@ __device__ __forceinline__ uint32_t frag_off(int kb, int t, int c4) {
 // token t in every block, so each warp reads one token's block row as whole
 // contiguous L2 lines; eight blocks are in flight before any is converted.
 // Tokens t >= T get zeros (the MMA reduces against all eight token columns).
-__device__ __noinline__ void build_frags(const ActSrc a, uint32_t mask) {
+// Blocks in ssq_mask (a subset of mask, residual input only) also get their
+// RMSNorm sum-of-squares partial: warp t sums token t's 128 values of the
+// block (before gamma) and stores it as ssq[which][kb][t].
+__device__ __noinline__ void build_frags(const ActSrc a, uint32_t mask, uint32_t ssq_mask = 0, int which = 0) {
     const Ctx c = make_ctx();
     unsigned char *fr = c.sm + SM_SCRATCH;
     const int t = c.tid >> 5, c4 = c.lane;
@@ -870,6 +884,12 @@ __device__ __noinline__ void build_frags(const ActSrc a, uint32_t mask) {
             if (kb[u] < 0) break;
             const float4 v = fx ? make_float4(from_fx(x0[u].x), from_fx(x0[u].y), from_fx(x1[u].x), from_fx(x1[u].y))
                                 : xf[u];
+            if (live && ((ssq_mask >> kb[u]) & 1u)) {  // warp-uniform
+                float q = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+                for (int o = 16; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+                if (c4 == 0) __stcg(c.m->ssq + (which * MK_MAXKB + kb[u]) * MK_MAXT + t, q);
+            }
             *reinterpret_cast<uint2 *>(fr + o_tc + kb[u] * 2048) =
                 make_uint2(pack_f16(v.x * g[u].x, v.y * g[u].y), pack_f16(v.z * g[u].z, v.w * g[u].w));
         }
@@ -1980,17 +2000,20 @@ __device__ __noinline__ void consumer() {
         const int l = p.mode ? p.layer : li;
         const DLayer &L = c.misc->L[li & 1];
         RouteSm *rt = &c.rt[li & 1];
-        // descriptors of the next layer, read by the producer once it gets there
-        // (it cannot pass this layer's tiles before these stores are done)
-        if (p.mode == 0 && li + 1 < nl) copy_layer(c, &c.misc->L[(li + 1) & 1], m.layers + li + 1);
         // ---- QKV
         {
             ActSrc a{m.res, nullptr, m.H, L.attn_norm};
             int b, e;
             split_range(stage_total(m, ST_QKV, L, rt), c.G, c.cta, b, e);
-            if (f32path) build_act32(a, m.H);
-            else build_frags(a, needed_kb(b, e, L.qkv));
-            ssq_block(c, 0);
+            if (f32path) {
+                build_act32(a, m.H);
+                ssq_block(c, 0);
+            } else {
+                // the owners of the first row group's tiles cover every block
+                // once: they also store the blocks' sum-of-squares partials
+                const int nkc = L.qkv.n_kc;
+                build_frags(a, needed_kb(b, e, L.qkv), b < nkc ? needed_kb(b, min(e, nkc), L.qkv) : 0u, 0);
+            }
             zero_slice(c, m.sh_acc, (long long)MK_MAXT * 2 * m.I);
             zero_slice(c, m.ea_acc, (long long)MK_MAXT * m.K * 2 * m.I);
             bar_consumers();
@@ -2022,14 +2045,21 @@ __device__ __noinline__ void consumer() {
         {
             ActSrc a{m.res, nullptr, m.H, L.moe_norm};
             mark(c, ST_ROUTER * 16 + 8);
-            if (f32path) build_act32(a, m.H);
-            else build_frags(a, chunk_kb_mask(c, m.H));
-            ssq_block(c, 1);
+            if (f32path) {
+                build_act32(a, m.H);
+                ssq_block(c, 1);
+            } else {
+                build_frags(a, chunk_kb_mask(c, m.H), ssq_owner_mask(c, m.H), 1);
+            }
             bar_consumers();
             mark(c, ST_ROUTER * 16 + 0);
             ci = cons_gemv(ST_ROUTER, &(L), rt, ci);
             grid_arrive(c);
             ci = cons_gemv(ST_SHA, &(L), rt, ci);
+            // descriptors of the next layer, copied while the barrier settles.
+            // The producer reads them only after this layer's routing, which
+            // these threads publish after the copy.
+            if (p.mode == 0 && li + 1 < nl) copy_layer(c, &c.misc->L[(li + 1) & 1], m.layers + li + 1);
             if (!grid_wait(c, 5)) return;
             mark(c, ST_EXPA * 16 + 3);
             route_layer(&L, rt);
