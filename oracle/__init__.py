@@ -26,9 +26,11 @@ K/V entries are stored in the cache dtype (bf16 or fp32) before attention reads
 them back.
 
 Parity status of each function is stated in its docstring; the pins live in
-``tests/test_oracle_pins.py``.  ``stack_forward`` composes pinned parts but has
-no printed worked example for this model: parity unpinned beyond the invariants
-(block verification = sequential decode, MoE reductions, accept rule).
+``tests/test_oracle_pins.py``.  ``stack_forward`` composes pinned parts; the
+pages print no worked example for this model, so it is pinned through special
+cases: with every O and down projection zero the stack reduces to final RMSNorm
++ LM head on the embeddings (checked against torch), an appended identity layer
+changes nothing, and block verification equals sequential decode.
 """
 from __future__ import annotations
 
@@ -433,7 +435,7 @@ def stack_forward(tokens: Sequence[int], embed: np.ndarray, layers: Sequence[Lay
     or a [V][H] fp64 array; kv_ctx[l] = (k_ctx, v_ctx) for layer l.
     Returns dict(logits [T][V], argmax [T], accepted, layers=[info...]).
     ``route_hook_factory(l)`` gives the per-layer hook (see ``layer_forward``).
-    Parity unpinned beyond the invariants named in the module docstring.
+    Pinned through the special cases named in the module docstring.
     """
     T = len(tokens)
     x = embed(np.asarray(tokens)) if callable(embed) else np.asarray(embed)[np.asarray(tokens)]

@@ -382,3 +382,57 @@ def test_stack_accept_and_argmax_consistency():
                               model.final_norm.numpy().astype(np.float64),
                               helpers.lm_head_lin(model), dims, kvs, cfg.ctx)
     assert rf["accepted"] == 3
+
+
+def _zero_layer_outputs(layer):
+    """Zero the O projection and every down projection: the layer becomes the identity."""
+    layer.w_o.data.zero_()
+    layer.w2.data.zero_()
+    if layer.ws2 is not None:
+        layer.ws2.data.zero_()
+
+
+def _stack(model, cfg, toks, n_layers=None):
+    n = cfg.n_layers if n_layers is None else n_layers
+    kv = synth.make_kv(cfg, "cpu")
+    return oracle.stack_forward(toks, helpers.embed_fn(model),
+                                [helpers.layer_view(model, l) for l in range(n)],
+                                model.final_norm.numpy().astype(np.float64),
+                                helpers.lm_head_lin(model), helpers.oracle_dims(cfg),
+                                [helpers.kv_view(kv, l) for l in range(n)], cfg.ctx)
+
+
+def test_stack_identity_layers_reduce_to_final_norm_and_lm_head():
+    # With every O projection and every down projection zero, both residual
+    # branches add nothing and the stack's logits are the LM head applied to the
+    # RMS-normalised embeddings: computed here with torch's own bf16 decoding
+    # and a plain matrix product.  A dropped residual, a second norm or a wrong
+    # gamma changes the result.
+    cfg = synth.tiny_config(n_layers=2, vocab=300, T=4, ctx=64, gamma_jitter=0.1)
+    model = synth.make_model(cfg, "cpu")
+    for lay in model.layers:
+        _zero_layer_outputs(lay)
+    toks = [7, 123, 5, 299]
+    r = _stack(model, cfg, toks)
+    e = model.embed[torch.tensor(toks)].to(torch.float64)
+    g = model.final_norm.to(torch.float64)
+    xn = e / torch.sqrt((e * e).mean(dim=1, keepdim=True) + cfg.rms_eps) * g
+    want = (xn @ model.lm_head.to(torch.float64).T).numpy()
+    assert np.allclose(r["logits"], want, rtol=1e-12, atol=1e-12)
+    assert np.allclose(r["x_final"], e.numpy(), rtol=0, atol=0)
+    assert np.array_equal(r["argmax"], np.argmax(want, axis=1))
+
+
+def test_stack_appended_identity_layer_changes_nothing():
+    # Layer l of the stack is applied once and in order: a two-layer stack
+    # whose second layer is the identity gives the one-layer stack's result,
+    # while a second live layer moves it.
+    cfg = synth.tiny_config(n_layers=2, vocab=300, T=3, ctx=64)
+    model = synth.make_model(cfg, "cpu")
+    toks = [11, 42, 250]
+    one = _stack(model, cfg, toks, n_layers=1)
+    two_live = _stack(model, cfg, toks)
+    _zero_layer_outputs(model.layers[1])
+    two_ident = _stack(model, cfg, toks)
+    assert np.allclose(two_ident["logits"], one["logits"], rtol=1e-13, atol=1e-13)
+    assert not np.allclose(two_live["logits"], one["logits"], rtol=1e-6, atol=1e-6)
