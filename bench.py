@@ -20,6 +20,7 @@ is the sum of tokens over ranks divided by the slowest rank's time.
 """
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -52,10 +53,19 @@ def measured_peaks():
         return None
 
 
+def _code_only(text):
+    """C++ source without its comments and with whitespace collapsed: what the
+    compiled kernel depends on, so that editing a comment keeps a stored figure."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("mk_kernel.cu", "mk_internal.h", "mk_api.cu"):
-        h.update(open(os.path.join(ROOT, "latency_moe_decode_persistent_gb300", "csrc", f), "rb").read())
+        with open(os.path.join(ROOT, "latency_moe_decode_persistent_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -229,6 +229,16 @@ __device__ __forceinline__ float from_fx(long long v) {
 __device__ __forceinline__ void red_add(long long *p, long long v) {
     atomicAdd(reinterpret_cast<unsigned long long *>(p), (unsigned long long)v);
 }
+// arrival at a counter with release semantics at GPU scope: every write this
+// CTA made before the preceding CTA barrier is visible to a thread whose
+// acquire load sees the new count (the barrier orders the other threads'
+// writes before this thread's release)
+__device__ __forceinline__ void arrive_release(unsigned long long *p) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(p) : "memory");
+}
+__device__ __forceinline__ void arrive_release(int *p) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p) : "memory");
+}
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
 // byte address of (row, byte) inside a TMA box stored with the 128-byte swizzle
@@ -379,9 +389,10 @@ __device__ void mbar_wait_drain(uint64_t *b, uint32_t parity, const Ctx &c) {
         if ((long long)(gtimer() - t0) > c.timeout) return;
     }
 }
-// spins of one thread on a counter in global memory: polls are spaced by a
-// short sleep after the first few so that many CTAs polling one line leave
-// the L2 slice that holds it free for other traffic
+// spins of one thread on a counter in global memory.  Each poll is one
+// acquire load that waits for its answer, so a CTA keeps at most one request
+// to the line in flight; a sleep between polls (64 ns) measured no better.
+// Timeout and abort are checked every 16 polls.
 __device__ bool spin_ge_u64(unsigned long long *a, unsigned long long target, const Ctx &c,
                             int where) {
     uint64_t t0 = 0;
@@ -389,7 +400,6 @@ __device__ bool spin_ge_u64(unsigned long long *a, unsigned long long target, co
         unsigned long long v;
         asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
         if (v >= target) return true;
-        if (it >= 4) __nanosleep(64);
         if ((it & 15) == 15) {
             if (aborted_global(c)) return false;
             uint64_t now = gtimer();
@@ -407,7 +417,6 @@ __device__ bool spin_ge_s32(int *a, int target, const Ctx &c, int where) {
         int v;
         asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
         if (v >= target) return true;
-        if (it >= 4) __nanosleep(64);
         if ((it & 15) == 15) {
             if (aborted_global(c)) return false;
             uint64_t now = gtimer();
@@ -429,19 +438,21 @@ __device__ __noinline__ void grid_arrive_nc() {
         const Params &p = *c.p;
         if (p.stage_trace && nbar <= p.stage_cap)
             p.stage_trace[((long long)c.cta * p.stage_cap + nbar - 1) * 2] = gtimer();
-        __threadfence();
         // test hook (mk_debug_skip_barrier): CTA 0 withholds one arrival so that
         // every other CTA's bounded wait runs out
-        if (!(p.skip_barrier == nbar && c.cta == 0)) atomicAdd(&c.ctrl->bar_count, 1ull);
+        if (!(p.skip_barrier == nbar && c.cta == 0)) arrive_release(&c.ctrl->bar_count);
     }
 }
 __device__ __noinline__ bool grid_wait_nc(int where) {
     const Ctx c = make_ctx();
     if (c.tid == 0) {
         const int nbar = c.misc->nbar;
-        bool ok = !aborted_global(c);
-        if (ok) ok = spin_ge_u64(&c.ctrl->bar_count, c.misc->base + (unsigned long long)nbar * c.G, c, where);
-        __threadfence();
+        // the abort flag is read alongside the first poll, not before it; the
+        // acquire loads of the poll order every later read of other CTAs' data
+        // (all of which goes through L2) after their arrivals
+        const int ab = *(volatile int *)&c.ctrl->abort;
+        bool ok = spin_ge_u64(&c.ctrl->bar_count, c.misc->base + (unsigned long long)nbar * c.G, c, where);
+        if (ab) *(volatile int *)&c.misc->abort = 1;
         c.misc->gs_ok = ok && !aborted(c);
         const Params &p = *c.p;
         if (p.stage_trace && nbar <= p.stage_cap)
@@ -1883,10 +1894,8 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     if (!u.active) return ci;
     if (c.tid == 0) {
         bool ok = !aborted(c);
-        __threadfence();
-        atomicAdd(m.att_cnt + l * m.Hkv + u.g, 1);
+        arrive_release(m.att_cnt + l * m.Hkv + u.g);
         if (ok) ok = spin_ge_s32(m.att_cnt + l * m.Hkv + u.g, c.nsplit, c, 220);
-        __threadfence();
         c.misc->gs_ok = ok;
     }
     bar_consumers();
