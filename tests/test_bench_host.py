@@ -1,0 +1,42 @@
+"""Host-side pieces of the bench that need no GPU: the key that ties a stored
+ncu traffic figure to the kernel code it was measured on, and the algorithmic
+byte count the roofline divides by."""
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+def test_code_key_ignores_comments_and_layout_only():
+    a = "int f(int x) {\n    // twice\n    return 2 * x; /* doubled */\n}\n"
+    b = "int f(int x) { return 2 * x; }  // a different comment\n"
+    c = "int f(int x) {\n    return 3 * x;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+
+
+def test_stored_traffic_matches_current_code_or_is_dropped():
+    # the committed figure is reported only while the kernel code matches the
+    # hash stored beside it
+    t = bench.ncu_traffic()
+    assert t is None or 0.9e10 < t < 2.0e10
+
+
+def test_algorithmic_bytes_of_the_43_layer_workload():
+    # The roofline's numerator, written out from the layer shapes (FP8 codes plus
+    # one fp32 scale per 128 inputs and output row; bf16 router, embedding and LM
+    # head; bf16 KV at ctx 2048; T = 6):
+    qkv = 5120 * 4096 + 32 * 5120 * 4
+    o = 4096 * 4096 + 32 * 4096 * 4
+    router = 384 * 4096 * 2 + 384 * 4
+    norms = 2 * 4096 * 4
+    expert = 2 * (512 * 4096 + 32 * 512 * 4) + (4096 * 512 + 4 * 4096 * 4)
+    kv = 2048 * 4 * 128 * 2 * 2 + 6 * 4 * 128 * 2 * 2
+    per_layer = qkv + o + router + norms + expert + kv
+    once = 6 * 4096 * 2 + 4096 * 4 + 129280 * 4096 * 2 + 6 * 129280 * 4
+    distinct = 1874  # routed experts over the 43 layers of the bench's step
+    want = 43 * per_layer + distinct * expert + once
+    from latency_moe_decode_persistent_gb300 import synth
+    cfg = synth.stack_config(T=6, ctx=2048)
+    assert bench.algorithmic_bytes(cfg, distinct, 2048) == want == 15491394048
