@@ -39,6 +39,15 @@ WORKLOAD = ("43-layer FP8 (e4m3, 1x128 scales) MoE stack: H 4096, 32 q / 4 kv he
             "1 stream, T=6 (k=5 drafts, 0.83 agreement), ctx 2048 bf16 KV in 64-token pages; seed 3")
 
 
+def workload_of(cfg):
+    """The workload string of a run: the default one, or the same stack with the
+    layer count and block size the run overrode."""
+    if cfg.n_layers == 43 and cfg.T == 6:
+        return WORKLOAD
+    return WORKLOAD.replace("43-layer", "%d-layer" % cfg.n_layers).replace(
+        "T=6 (k=5 drafts", "T=%d (k=%d drafts" % (cfg.T, cfg.T - 1))
+
+
 def rank_info():
     r = int(os.environ.get("RANK", "0"))
     w = int(os.environ.get("WORLD_SIZE", "1"))
@@ -332,7 +341,7 @@ def run_mk(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8e4m3 weights x f16 activations -> fp32 (bf16 LM head), int64 fixed-point reductions",
         "data": "synthetic (seeded random weights of the named architecture)",
-        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": T,
+        "config": {"workload": workload_of(cfg), "global_batch": world, "seq_len": T,
                    "parallelism": "replicas (1 stream per GPU)" if world > 1 else "single GPU",
                    "l2": "no flush: each step streams ~%.1f GB, far above the 129 MB L2" % (bytes_step / 1e9)},
         "step_us": {"mean": round(mean_ms * 1e3, 2), "median": round(statistics.median(step_ms) * 1e3, 2),
@@ -341,7 +350,9 @@ def run_mk(args):
         "tokens_per_step": round(tok_per_step, 4), "accepted_mean": round(acc_mean, 4),
         "distinct_experts_per_layer": round(distinct / cfg.n_layers, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(),
+                     "frac": round(achieved / peak, 4),
+                     # the stored figure belongs to the default workload only
+                     "traffic": ncu_traffic() if workload_of(cfg) == WORKLOAD else None,
                      "kernel": "mk_step_kernel", "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes_per_launch": int(bytes_step)},
         "e2e": {"value": round(e2e_value, 3), "unit": "tok/s",
