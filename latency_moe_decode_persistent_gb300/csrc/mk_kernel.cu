@@ -26,9 +26,10 @@
 //               (2^-32) int64 accumulator.  Integer adds make every cross-CTA
 //               reduction order-independent, so the step is bitwise deterministic.
 // RMSNorm is folded: GEMVs consume gamma*x and the consumer of their result
-// divides by rms(x), whose sum of squares is computed by 32 CTAs in parallel.
-// Grid barriers (monotonic counter, acquire/release) separate the stages; every
-// wait is bounded by %globaltimer and turns into a status code.
+// divides by rms(x); the per-block sums of squares are formed while the
+// activation fragments are built.  Grid barriers separate the stages: one
+// release reduction per CTA on a monotonic counter, acquire polls to wait.
+// Every wait is bounded by %globaltimer and turns into a status code.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -1243,7 +1244,9 @@ __device__ __forceinline__ void zero_slice(const Ctx &c, long long *p, long long
     (void)c;
     zero_slice_nc(p, n);
 }
-// sum of squares of 128-column block `kb` of the residual for every token
+// sum of squares of 128-column block kb = (this CTA's index) of the residual
+// for every token, for the final norm and the all-fp32 build; elsewhere the
+// partials are formed in build_frags
 __device__ __noinline__ void ssq_block_nc(int which) {
     const Ctx c = make_ctx();
     const DModel &m = *c.m;
