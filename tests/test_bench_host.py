@@ -40,3 +40,13 @@ def test_algorithmic_bytes_of_the_43_layer_workload():
     from latency_moe_decode_persistent_gb300 import synth
     cfg = synth.stack_config(T=6, ctx=2048)
     assert bench.algorithmic_bytes(cfg, distinct, 2048) == want == 15491394048
+
+
+def test_workload_string_follows_the_run():
+    # the default run is described by the default workload string (the one the
+    # stored traffic figure belongs to); a run with fewer layers or another block
+    # size says so
+    from latency_moe_decode_persistent_gb300 import synth
+    assert bench.workload_of(synth.stack_config()) == bench.WORKLOAD
+    w = bench.workload_of(synth.stack_config(n_layers=2, T=4))
+    assert w.startswith("2-layer") and "T=4 (k=3 drafts" in w and w != bench.WORKLOAD
