@@ -18,7 +18,8 @@ reading of the workload description that goes with them: pre-norm residual
 blocks, GQA attention with rotate-half RoPE over a paged KV cache, a sigmoid
 router whose bias only steers selection, top-K with weights normalised to 1,
 SwiGLU experts plus one shared expert, RMSNorm + LM head + greedy argmax, and
-the longest-accepted-prefix rule.  Every reading is listed in the design doc.
+the longest-accepted-prefix rule.  Each of these readings is the plainest one
+the pages and the workload description support; none is printed on the pages.
 
 Arithmetic: every floating-point value is widened to fp64 and computed in fp64.
 The only deliberate roundings are the ones the method itself performs: the new
@@ -112,7 +113,10 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def round_to_f32(x: np.ndarray) -> np.ndarray:
-    """Round fp64 to the nearest binary32 value (ties to even), returned as fp64."""
+    """Round fp64 to the nearest binary32 value (ties to even), returned as fp64.
+
+    Used for the fp32 KV cache of the all-fp32 layer.  Pinned (hand-chosen
+    halfway values, normal and subnormal)."""
     return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
 
 
@@ -293,7 +297,9 @@ def route(logits: np.ndarray, bias: np.ndarray, top_k: int):
 
 
 def swiglu(w1: Linear, w3: Linear, w2: Linear, z: np.ndarray) -> np.ndarray:
-    """W2 (silu(W1 z) * (W3 z)) for rows of z [n][H] -> [n][H].  Pinned."""
+    """W2 (silu(W1 z) * (W3 z)) for rows of z [n][H] -> [n][H]: W1 is the gate
+    (through silu), W3 the up projection.  Pinned (a hand-computed case with
+    W1 != W3, in which swapping the two roles changes the result)."""
     return linear(w2, silu(linear(w1, z)) * linear(w3, z))
 
 
@@ -459,7 +465,9 @@ def kv_from_pool(kind: str, k_pool: np.ndarray, v_pool: np.ndarray,
     """Decode a stream's cached K/V (stored bits) and follow its page table.
 
     kind "bf16": pools hold uint16 bfloat16 bits; "f32": float32 values.
-    Returns (k_ctx, v_ctx), each fp64 [Hkv][ctx][d].
+    Returns (k_ctx, v_ctx), each fp64 [Hkv][ctx][d].  Pinned (a hand-built pool
+    whose entries name their page, head and slot, read through a permuted
+    page table).
     """
     dec = bf16_decode if kind == "bf16" else (lambda a: np.asarray(a, dtype=np.float64))
     P = k_pool.shape[2]

@@ -55,6 +55,22 @@ def test_bf16_round_ties_to_even():
     assert oracle.round_to_bf16(np.array([1 + 2 ** -8 + 2 ** -30]))[0] == 1 + 2 ** -7
 
 
+def test_f32_round_ties_to_even():
+    # binary32 keeps 24 significant bits: 1 + 2^-24 lies halfway between 1 and
+    # 1 + 2^-23, and the tie goes to the even significand (1)
+    assert oracle.round_to_f32(np.array([1 + 2 ** -24]))[0] == 1.0
+    # 1 + 3*2^-24 lies halfway between 1 + 2^-23 and 1 + 2^-22: even is 1 + 2^-22
+    assert oracle.round_to_f32(np.array([1 + 3 * 2 ** -24]))[0] == 1 + 2 ** -22
+    # just above a halfway point rounds up
+    assert oracle.round_to_f32(np.array([1 + 2 ** -24 + 2 ** -40]))[0] == 1 + 2 ** -23
+    # subnormal grid 2^-149: 3*2^-150 is halfway between 2^-149 and 2^-148 -> 2^-148
+    assert oracle.round_to_f32(np.array([3 * 2.0 ** -150]))[0] == 2.0 ** -148
+    # 2^-150 is halfway between 0 and 2^-149 -> 0 (even)
+    assert oracle.round_to_f32(np.array([2.0 ** -150]))[0] == 0.0
+    # a value binary32 holds exactly is unchanged
+    assert oracle.round_to_f32(np.array([0.1875]))[0] == 0.1875
+
+
 # ---------------------------------------------------------------- linear/dequant
 def test_fp8_linear_exact_on_integer_weights():
     # codes for the integers 1..8 and their negatives, power-of-two block scales:
@@ -221,6 +237,31 @@ def test_paged_gather_follows_table():
         assert np.array_equal(seq[:, p], pool[pt[p // 4], :, p % 4])
 
 
+def test_kv_from_pool_hand_built_table():
+    # 3 physical pages of 2 positions, 2 kv heads, head dim 2; entry
+    # (page p, head h, slot i) holds (100h + 10p + i, -(100h + 10p + i)).
+    P, Hkv, d = 2, 2, 2
+    pool = np.zeros((3, Hkv, P, d), dtype=np.float32)
+    for p in range(3):
+        for h in range(Hkv):
+            for i in range(P):
+                pool[p, h, i] = (100 * h + 10 * p + i, -(100 * h + 10 * p + i))
+    vpool = pool + 0.5
+    # logical page 0 -> physical 2, 1 -> 0, 2 -> 1; five cached positions
+    pt = np.array([2, 0, 1])
+    k, v = oracle.kv_from_pool("f32", pool, vpool, pt, 5)
+    want_h0 = [20, 21, 0, 1, 10]
+    want_h1 = [120, 121, 100, 101, 110]
+    assert k.shape == (2, 5, 2)
+    assert k[0, :, 0].tolist() == want_h0 and k[1, :, 0].tolist() == want_h1
+    assert k[0, :, 1].tolist() == [-x for x in want_h0]
+    assert v[1, :, 0].tolist() == [x + 0.5 for x in want_h1]
+    # the same pool stored as bf16 bits (small integers are exact in bf16)
+    bits = torch.from_numpy(pool).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    kb, _ = oracle.kv_from_pool("bf16", bits, bits, pt, 3)
+    assert kb[0, :, 0].tolist() == [20, 21, 0] and kb[1, :, 1].tolist() == [-120, -121, -100]
+
+
 # ----------------------------------------------------------------------- router
 def test_router_brute_force_16_choose_2():
     for trial in range(20):
@@ -332,6 +373,23 @@ def test_moe_identical_experts_reduce_to_dense_swiglu():
     out, info = oracle.layer_forward(x, lv, dims, kc, vc, cfg.ctx)
     dense = oracle.swiglu(*lv.expert(0), info["z"])
     assert np.allclose(out - info["h"], dense, rtol=1e-12, atol=1e-13)
+
+
+def test_swiglu_gate_and_up_roles_hand_case():
+    # H = 2, I = 1: W1 (gate) reads z_0 with weight 2, W3 (up) reads z_1 with
+    # weight 3, W2 writes the intermediate to the two outputs with weights 1
+    # and -0.5.  For z = (1, 1): gate 2, up 3, intermediate silu(2) * 3 =
+    # 6 / (1 + e^-2) = 5.284782467867294.  Swapping gate and up would give
+    # silu(3) * 2 = 5.7154447609345995.  For z = (-1, 2): gate -2, up 6,
+    # intermediate -12 / (1 + e^2) = -1.4304350642654104.
+    w1 = oracle.Linear("f32", np.array([[2.0, 0.0]], dtype=np.float32))
+    w3 = oracle.Linear("f32", np.array([[0.0, 3.0]], dtype=np.float32))
+    w2 = oracle.Linear("f32", np.array([[1.0], [-0.5]], dtype=np.float32))
+    y = oracle.swiglu(w1, w3, w2, np.array([[1.0, 1.0], [-1.0, 2.0]]))
+    want = np.array([[5.284782467867294, -2.642391233933647],
+                     [-1.4304350642654104, 0.7152175321327052]])
+    assert np.allclose(y, want, rtol=1e-15, atol=0)
+    assert not np.allclose(y[0, 0], 5.7154447609345995, rtol=1e-3)
 
 
 def test_moe_linear_in_weights():
