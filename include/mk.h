@@ -57,7 +57,10 @@ typedef enum {
     MK_ERR_TIMEOUT = -4,      /* a device-side wait ran past timeout_ms                */
     MK_ERR_CUDA = -5,         /* a CUDA runtime call failed                            */
     MK_ERR_BAD_STATE = -6,    /* call not valid in the current state                   */
-    MK_ERR_BAD_INPUT = -7     /* device-side input check failed (positions, page table)*/
+    MK_ERR_BAD_INPUT = -7,    /* device-side input check failed (positions, page table)*/
+    MK_ERR_RANGE = -8         /* a value left the kernel's number range: an f16 GEMV    */
+                              /* input beyond 65504 (or NaN), or a partial sum of       */
+                              /* magnitude >= 2^31 for the 2^-32 fixed-point sums       */
 } mk_status;
 
 /* storage types of weights and of the KV cache */
@@ -156,7 +159,12 @@ typedef struct mk_state mk_state;
  * persistent CTAs co-resident), build TMA descriptors for every weight matrix,
  * precompute the RoPE table (fp64 on the host, stored fp32) and allocate the
  * workspace.  Weights must stay valid until mk_destroy.  On success *out owns
- * the state.  Errors: MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_NOMEM, MK_ERR_CUDA. */
+ * the state.  Errors: MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_NOMEM, MK_ERR_CUDA.
+ * Passage: ezolabs "DeepSeek-V4.1-Flash breaks 1,000 tokens per second for one
+ * user", section "What NVIDIA shipped, and why B300 was refused": the megakernel
+ * keeps one persistent block per SM and refuses an SM count it was not built
+ * for rather than falling back; here a device other than CC 10.3, or a grid
+ * that cannot be fully co-resident, returns MK_ERR_UNSUPPORTED. */
 mk_status mk_create(const mk_model_desc *desc, const mk_weights *weights, mk_state **out);
 
 /* One verify step for one stream.
@@ -166,7 +174,16 @@ mk_status mk_create(const mk_model_desc *desc, const mk_weights *weights, mk_sta
  *   out_logits    dev float32 [T][vocab]
  *   out_accepted  dev int32 [1]: n = longest prefix of drafts with d_i = argmax_{i-1}
  *   out_argmax    dev int32 [T] or NULL
- * Requires vocab > 0 and 1 <= T <= max_T. */
+ * Requires vocab > 0 and 1 <= T <= max_T.  Device-side errors
+ * (MK_ERR_BAD_INPUT, MK_ERR_TIMEOUT, MK_ERR_RANGE) land in the status word.
+ * Passages: al-engr "Why one GB300 doesn't beat 4x RTX PRO 6000 at
+ * single-stream decode", section "The decomposition" (tokens per verify step =
+ * accepted drafts + 1, so the step reports the accepted-prefix count n and the
+ * argmax a_n that becomes the next d_0), and section "Where the 11.2 ms goes"
+ * (the per-step work -- 43 MoE layers, decode attention, dense projections,
+ * router top-k, lm_head and the rejection kernel -- that this one launch
+ * replaces); ezolabs, section "How we got here" (drafted tokens are verified
+ * together in one block). */
 mk_status mk_decode_step(mk_state *st, const int32_t *draft_tokens, int T,
                          const int32_t *positions, const mk_kv_cache *kv,
                          float *out_logits, int32_t *out_accepted, int32_t *out_argmax,
@@ -184,14 +201,18 @@ mk_status mk_decode_step(mk_state *st, const int32_t *draft_tokens, int T,
  * alone.  This build runs the streams one after another on `stream` (one launch
  * per stream, each streaming the weights once); each counts as one step in
  * mk_get_stats.  Requires vocab > 0, 1 <= T <= max_T, n_streams >= 1 and a page
- * table with at least n_streams rows. */
+ * table with at least n_streams rows.
+ * Passage: ezolabs, section "Speed", table "Gain by number of streams" (the
+ * megakernel measured at 1 to 16 concurrent streams). */
 mk_status mk_decode_batch(mk_state *st, int n_streams, const int32_t *draft_tokens, int T,
                           const int32_t *positions, const mk_kv_cache *kv, float *out_logits,
                           int32_t *out_accepted, int32_t *out_argmax, void *stream);
 
 /* The same step through HOST buffers: copies the tokens and positions in, runs
  * the step, copies the results out and synchronizes the stream.  out_logits and
- * out_argmax may be NULL.  Returns the device status of the step. */
+ * out_argmax may be NULL.  Returns the device status of the step.
+ * Passage: as mk_decode_step; this is the end-to-end form a serving loop calls
+ * (al-engr, section "The decomposition": tokens/s counts whole verify steps). */
 mk_status mk_decode_step_host(mk_state *st, const int32_t *h_tokens, int T,
                               const int32_t *h_positions, const mk_kv_cache *kv,
                               float *h_logits, int32_t *h_accepted, int32_t *h_argmax,
@@ -201,7 +222,11 @@ mk_status mk_decode_step_host(mk_state *st, const int32_t *h_tokens, int T,
  *   hidden_in, hidden_out  dev float32 [T][H] (may not alias)
  *   out_topk_idx           dev int32 [T][top_k] or NULL (selected experts, key order)
  *   out_topk_w             dev float32 [T][top_k] or NULL (their weights)
- * K/V of the T tokens are written into layer `layer` of the cache. */
+ * K/V of the T tokens are written into layer `layer` of the cache.
+ * Passage: al-engr, section "Where the 11.2 ms goes", kernel table (per layer:
+ * q/kv norm, RoPE and KV insert, decode attention, dense projections, router
+ * top-k, MoE experts); section "Tier 2: the fusion program" (one persistent
+ * kernel per decoder layer). */
 mk_status mk_layer_forward(mk_state *st, int layer, const float *hidden_in, int T,
                            const int32_t *positions, const mk_kv_cache *kv,
                            float *hidden_out, int32_t *out_topk_idx, float *out_topk_w,
@@ -215,25 +240,30 @@ mk_status mk_layer_forward(mk_state *st, int layer, const float *hidden_in, int 
  * pool or fail under memory pressure).  The pages have no counterpart: it is
  * an integration entry point.
  *
- * Runs layer `layer`'s computation exactly as mk_layer_forward does (same
- * kernel, same results) for a model described by desc (n_layers is ignored)
- * with that layer's weights lw; the KV pools, page table and positions are the
- * caller's as in mk_layer_forward, with ctx = positions[0] also passed on the
- * host.  All other state -- the model block, TMA descriptors, RoPE rows,
- * control block and accumulators -- lives in one file-scope device array of
- * 24 MiB that every device which loads this library holds until the process
- * exits.  A model whose working set does not fit returns MK_ERR_UNSUPPORTED
- * (a layer of hidden 4096, 32/4 heads of 128, 384 experts of width 512 takes
- * about 23 MiB).  out_status (dev int32 [1], may be NULL) receives the device
- * status (MK_OK, MK_ERR_BAD_INPUT or MK_ERR_TIMEOUT) in stream order.
+ * Runs one decoder layer with the weights lw, exactly as mk_layer_forward does
+ * (same kernel, same results), for a model described by desc (n_layers is
+ * ignored).  The KV pools, page table and positions are the caller's as in
+ * mk_layer_forward.  ctx must equal positions[0]: the host stages the RoPE
+ * rows of positions ctx .. ctx+T-1 only, and the kernel refuses a launch whose
+ * positions[0] differs (MK_ERR_BAD_INPUT in out_status, before any stage runs).
+ * All other state -- the model block, TMA descriptors, RoPE rows, control block
+ * and accumulators -- lives in one file-scope device array of 24 MiB that every
+ * device which loads this library holds until the process exits.  A model whose
+ * working set does not fit returns MK_ERR_UNSUPPORTED (a layer of hidden 4096,
+ * 32/4 heads of 128, 384 experts of width 512 takes about 23 MiB).  out_status
+ * (dev int32 [1], may be NULL) receives the device status (MK_OK,
+ * MK_ERR_BAD_INPUT, MK_ERR_TIMEOUT or MK_ERR_RANGE) in stream order.
  *
  * The first call on a device does that device's set-up (finding the array's
  * device address, the kernel's shared-memory attribute); make it with the
- * device current and before any stream capture.  Every call reuses the same
- * array, so calls that may overlap on the device (different streams without
- * ordering, several host threads) race and give wrong results: serialise them.
- * Each call clears the control block it needs; nothing else must start at zero.
- * No call allocates device or host memory. */
+ * device current.  Each call stages its tables into the array with
+ * stream-ordered copies from host memory, so it must not be made while
+ * `stream` is being captured into a CUDA graph: it returns MK_ERR_UNSUPPORTED
+ * then.  Every call reuses the same array, so calls that may overlap on the
+ * device (different streams without ordering, several host threads) race and
+ * give wrong results: serialise them.  Each call clears the control block it
+ * needs; nothing else must start at zero.  No call allocates device or host
+ * memory. */
 mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const mk_layer_weights *lw,
                                    void *k_pool, void *v_pool, const int32_t *page_table,
                                    int n_pages, const float *hidden_in, int T, int ctx,
@@ -242,10 +272,14 @@ mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const mk_layer_wei
                                    int32_t *out_status, void *stream);
 
 /* Record, on every later mk_decode_step, each layer's selected experts into
- * trace (dev int32 [n_layers][T][top_k], key order); NULL turns it off.  The
- * buffer must stay valid while tracing is on.  Used to check routing layer by
- * layer against a reference. */
-mk_status mk_set_routing_trace(mk_state *st, int32_t *trace);
+ * idx_trace (dev int32 [n_layers][T][top_k], key order) and their normalised
+ * weights into w_trace (dev float32 [n_layers][T][top_k]); either may be NULL,
+ * both NULL turns tracing off.  The buffers must stay valid while tracing is
+ * on.  Used to check routing layer by layer against a reference.
+ * Passage: al-engr, section "Where the 11.2 ms goes" (the router top-k runs
+ * once per layer); the router's selection and weights are the quantities the
+ * per-layer check compares. */
+mk_status mk_set_routing_trace(mk_state *st, int32_t *idx_trace, float *w_trace);
 
 /* Timeline of later launches: for every CTA c and grid barrier b < capacity,
  * times[(c*capacity + b)*2] is the %globaltimer value (ns) when the CTA arrived
@@ -254,25 +288,39 @@ mk_status mk_set_routing_trace(mk_state *st, int32_t *trace);
  * between barriers s-1 and s, so this splits the single launch into stages.
  * events (dev uint64 [grid][1024][2], or NULL) receives (event id, time) pairs
  * at points inside the stages: id = stage*16 + k, k = 0 inputs staged, 1 first
- * weight tile arrived, 2 last tile reduced, 3 routing started (attention:
- * 0 queries ready, 1 pages done, 2 group barrier passed, 3 merge done). */
+ * weight tile arrived, 2 last tile reduced, 3 routing started, 5 stage code
+ * entered, 6 activation fragments built, 7 first tile wait begins (attention:
+ * 0 queries ready, 1 pages done, 2 group barrier passed, 3 merge done).
+ * Passage: al-engr, section "Where the 11.2 ms goes" (a per-kernel time budget
+ * of one step); with one launch per step the budget has to come from inside
+ * the kernel. */
 mk_status mk_set_stage_trace(mk_state *st, uint64_t *times, int capacity, uint64_t *events);
 
 /* Test hook for the failure path: on every later launch, CTA 0 does not arrive
  * at grid barrier `barrier` (1-based, in launch order; 0 turns the hook off).
  * The other CTAs' waits then run out after timeout_ms, the launch ends with
  * MK_ERR_TIMEOUT in the device status and every CTA returns; nothing traps or
- * hangs.  mk_reset (with the hook off) restores a working state. */
+ * hangs.  mk_reset (with the hook off) restores a working state.
+ * Passage: ezolabs, section "The safety layer" (a watchdog restarts an engine
+ * whose megakernel stalls); here every device wait is bounded instead and a
+ * stall becomes a status. */
 mk_status mk_debug_skip_barrier(mk_state *st, int barrier);
 
 /* Synchronize the last stream used and return the device status of the last
- * step (MK_OK, MK_ERR_TIMEOUT or MK_ERR_BAD_INPUT). */
+ * step (MK_OK, MK_ERR_TIMEOUT, MK_ERR_BAD_INPUT or MK_ERR_RANGE).
+ * Passage: ezolabs, section "The safety layer" (stalls and divergence are
+ * detected and reported instead of passing silently). */
 mk_status mk_get_status(mk_state *st);
 
-/* Synchronize and copy the counters. */
+/* Synchronize and copy the counters.
+ * Passage: ezolabs, section "What NVIDIA shipped" (callers on the old interface
+ * silently ran the unfused path; `fused` and `launches_per_step` let a caller
+ * check that the fused kernel ran) and al-engr, section "The decomposition"
+ * (accepted_sum / steps + 1 is the tokens-per-step factor). */
 mk_status mk_get_stats(mk_state *st, mk_stats *out);
 
-/* Clear the device status, barrier epochs and counters (synchronous). */
+/* Clear the device status, barrier epochs and counters (synchronous).
+ * Passage: ezolabs, section "The safety layer" (recovery after a stall). */
 mk_status mk_reset(mk_state *st);
 
 /* Free the workspace.  Safe on NULL. */

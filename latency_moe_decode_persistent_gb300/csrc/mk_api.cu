@@ -34,6 +34,7 @@ struct mk_state {
     float *d_logits = nullptr;
     cudaStream_t last_stream = nullptr;
     int32_t *trace = nullptr;
+    float *wtrace = nullptr;
     unsigned long long *stage_trace = nullptr;
     int stage_cap = 0;
     unsigned long long *marks = nullptr;
@@ -182,6 +183,7 @@ const char *mk_status_string(mk_status s) {
         case MK_ERR_CUDA: return "CUDA runtime error";
         case MK_ERR_BAD_STATE: return "bad state";
         case MK_ERR_BAD_INPUT: return "device-side input check failed";
+        case MK_ERR_RANGE: return "value outside the kernel's number range";
     }
     return "unknown status";
 }
@@ -420,6 +422,7 @@ mk_status mk_decode_step(mk_state *st, const int32_t *draft_tokens, int T, const
     p.out_accepted = out_accepted;
     p.out_argmax = out_argmax;
     p.trace = st->trace;
+    p.wtrace = st->wtrace;
     return launch(st, p, stream);
 }
 
@@ -486,9 +489,10 @@ mk_status mk_layer_forward(mk_state *st, int layer, const float *hidden_in, int 
     return launch(st, p, stream);
 }
 
-mk_status mk_set_routing_trace(mk_state *st, int32_t *trace) {
+mk_status mk_set_routing_trace(mk_state *st, int32_t *idx_trace, float *w_trace) {
     if (!st) return MK_ERR_INVALID;
-    st->trace = trace;
+    st->trace = idx_trace;
+    st->wtrace = w_trace;
     return MK_OK;
 }
 
@@ -545,8 +549,9 @@ mk_status mk_reset(mk_state *st) {
 // ---------------------------------------------------------------------------
 // mk_layer_forward_noalloc: the same kernel in one-layer mode, for callers that
 // cannot allocate device memory (an allocator-less runtime, a plugin host that
-// owns all device memory, code that must not allocate after start-up or while
-// a CUDA graph is being captured).  Everything the launch needs besides the
+// owns all device memory, code that must not allocate after start-up).  Calls
+// stage their tables with copies from host memory, so they are refused during
+// stream capture.  Everything the launch needs besides the
 // caller's tensors -- the model block, the layer's TMA descriptors, the RoPE
 // rows of the step, the control block and all accumulators -- is carved out of
 // one file-scope device array, so no call allocates.
@@ -641,6 +646,15 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     if (d.timeout_ms <= 0) d.timeout_ms = 1000;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ret(fail(st, MK_ERR_CUDA, "no CUDA device"));
+    {
+        // the tables below are staged with copies from this call's stack: a
+        // captured graph would replay them from memory that no longer holds them
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(reinterpret_cast<cudaStream_t>(stream), &cs) != cudaSuccess)
+            return ret(fail(st, MK_ERR_CUDA, "cudaStreamIsCapturing failed"));
+        if (cs != cudaStreamCaptureStatusNone)
+            return ret(fail(st, MK_ERR_UNSUPPORTED, "mk_layer_forward_noalloc cannot be called during stream capture"));
+    }
     NoallocDevice *nd = nullptr;
     if ((r = noalloc_setup(st, dev, &nd)) != MK_OK) return ret(r);
     st->encode = nd->encode;
@@ -778,6 +792,7 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     p.hidden_out = hidden_out;
     p.out_idx = out_topk_idx;
     p.out_w = out_topk_w;
+    p.host_ctx1 = ctx + 1;  // the RoPE rows above exist for positions ctx .. ctx+T-1 only
     cudaError_t e = mk_launch(p, nd->grid, nd->smem, s, d.weight_dtype == MK_DT_F32);
     if (e != cudaSuccess) return ret(fail(st, MK_ERR_CUDA, "launch: %s", cudaGetErrorString(e)));
     if (out_status)

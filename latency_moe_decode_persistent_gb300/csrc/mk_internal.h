@@ -117,6 +117,8 @@ struct Params {
     int32_t *out_idx;
     float *out_w;
     int32_t *trace;                    // [L][T][K] routing trace or null
+    float *wtrace;                     // [L][T][K] routing weights trace or null
+    int host_ctx1;                     // 1 + the ctx the host staged tables for (0: no check)
     unsigned long long *stage_trace;   // [G][cap][2] barrier arrive/release times or null
     int stage_cap;
     unsigned long long *marks;         // [G][MK_MARKS][2] (event id, time) or null

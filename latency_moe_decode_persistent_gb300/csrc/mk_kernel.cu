@@ -45,6 +45,12 @@
 #define MK_F32_MODEL 0
 #endif
 
+// MK_L2PF 1: request the next layer's dense weights and KV pages into L2
+// during the current layer's O projection
+#ifndef MK_L2PF
+#define MK_L2PF 0
+#endif
+
 namespace {
 
 constexpr bool kF32 = MK_F32_MODEL != 0;
@@ -133,6 +139,20 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
             "r"(sa(dst)),
         "l"(src), "r"(bytes), "r"(sa(bar))
         : "memory");
+}
+// L2 prefetches (no shared memory, no completion): a box of a tensor map, or
+// a contiguous range (16-byte aligned, a multiple of 16 bytes)
+__device__ __forceinline__ void pf_l2_2d(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void pf_l2_3d(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
+                 "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void pf_l2_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void bar_consumers() {
     asm volatile("bar.sync 1, %0;" ::"n"(MK_NCWARPS * 32) : "memory");
@@ -364,6 +384,21 @@ __device__ void raise_err(const Ctx &c, int code, int where) {
     if (atomicCAS(&c.ctrl->status, 0, code) == 0) atomicExch(&c.ctrl->where, where);
     atomicExch(&c.ctrl->abort, 1);
 }
+// a value left the range of the kernel's number formats: an f16 GEMV input
+// beyond 65504 (or NaN), or a partial sum of magnitude 2^31 or more that the
+// 2^-32 fixed-point accumulators cannot hold.  The step stops with MK_ERR_RANGE
+// instead of returning infinities or wrapped sums.
+__device__ __noinline__ void range_err(int where) {
+    const Ctx c = make_ctx();
+    raise_err(c, MK_ERR_RANGE, where);
+}
+// nonzero if either half of an f16x2 word is infinite or NaN (exponent all ones)
+__device__ __forceinline__ uint32_t f16x2_bad(uint32_t w) {
+    return __vcmpeq2(w & 0x7c007c00u, 0x7c007c00u);
+}
+// nonzero unless |v| < 2^31 (NaN included)
+__device__ __forceinline__ uint32_t fx_bad(float v) { return !(fabsf(v) < 2147483648.0f); }
+
 // bounded wait on an mbarrier phase: first try inline, the rest out of line
 __device__ __noinline__ bool mbar_wait_slow(uint64_t *b, uint32_t parity, int where) {
     const Ctx c = make_ctx();
@@ -868,7 +903,7 @@ __device__ __noinline__ void build_frags(const ActSrc a, uint32_t mask, uint32_t
     const float *gm = a.gamma ? a.gamma + 4 * c4 : nullptr;
     const uint32_t o_tc = frag_off(0, t, c4);
     constexpr int B = 8;
-    uint32_t rest = mask;
+    uint32_t rest = mask, bad = 0;
     while (rest) {
         int kb[B];
         longlong2 x0[B], x1[B];
@@ -902,10 +937,12 @@ __device__ __noinline__ void build_frags(const ActSrc a, uint32_t mask, uint32_t
                 for (int o = 16; o; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
                 if (c4 == 0) __stcg(c.m->ssq + (which * MK_MAXKB + kb[u]) * MK_MAXT + t, q);
             }
-            *reinterpret_cast<uint2 *>(fr + o_tc + kb[u] * 2048) =
-                make_uint2(pack_f16(v.x * g[u].x, v.y * g[u].y), pack_f16(v.z * g[u].z, v.w * g[u].w));
+            const uint32_t w0 = pack_f16(v.x * g[u].x, v.y * g[u].y), w1 = pack_f16(v.z * g[u].z, v.w * g[u].w);
+            bad |= f16x2_bad(w0) | f16x2_bad(w1);
+            *reinterpret_cast<uint2 *>(fr + o_tc + kb[u] * 2048) = make_uint2(w0, w1);
         }
     }
+    if (bad) range_err(300 + which);
 }
 // f32 activations [MK_MAXT][K] for the FFMA path
 __device__ __noinline__ void build_act32(const ActSrc a, int K) {
@@ -988,24 +1025,36 @@ __device__ __forceinline__ void flush_mma(const Ctx &c, const Tgt &g, int row0, 
     const int r = c.lane >> 2, q = c.lane & 3;
     float w0, w1;
     const int o0 = tgt_off(g, 2 * q, c.T, w0), o1 = tgt_off(g, 2 * q + 1, c.T, w1);
+    uint32_t bad = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int o = (i & 1) ? o1 : o0;
         const float w = (i & 1) ? w1 : w0;
         const int row = row0 + (i >> 2) * 16 + r + ((i >> 1) & 1) * 8;
-        if (o >= 0 && row < g.row_limit) red_add(g.base + o + row, to_fx(acc[i] * w));
+        if (o >= 0 && row < g.row_limit) {
+            const float v = acc[i] * w;
+            bad |= fx_bad(v);
+            red_add(g.base + o + row, to_fx(v));
+        }
     }
+    if (bad) range_err(320 + g.st);
 }
 // FFMA layout: lane l holds row l of the warp's 32 rows, all tokens
 __device__ __forceinline__ void flush_f32(const Ctx &c, const Tgt &g, int row0, const float *acc) {
     int row = row0 + c.lane;
     if (row >= g.row_limit) return;
+    uint32_t bad = 0;
 #pragma unroll
     for (int t = 0; t < MK_MAXT; ++t) {
         float w;
         const int o = tgt_off(g, t, c.T, w);
-        if (o >= 0) red_add(g.base + o + row, to_fx(acc[t] * w));
+        if (o >= 0) {
+            const float v = acc[t] * w;
+            bad |= fx_bad(v);
+            red_add(g.base + o + row, to_fx(v));
+        }
     }
+    if (bad) range_err(320 + g.st);
 }
 
 // one 256-row x 128-byte tile of FP8 or bf16 weights against the f16 fragments;
@@ -1134,6 +1183,7 @@ __device__ __noinline__ void build_h_frags(const RouteSm *rt, int ex, bool f32pa
     unsigned char *fr = c.sm + SM_SCRATCH + frag_off(0, t, c4);
     const int nkb = m.I / 128;
     constexpr int B = 4;
+    uint32_t bad = 0;
     for (int kb0 = 0; kb0 < nkb; kb0 += B) {
         longlong2 av[B][2], bv[B][2];
 #pragma unroll
@@ -1158,9 +1208,12 @@ __device__ __noinline__ void build_h_frags(const RouteSm *rt, int ex, bool f32pa
                 h[2] = silu_mul(from_fx(av[u][1].x) * inv, from_fx(bv[u][1].x) * inv);
                 h[3] = silu_mul(from_fx(av[u][1].y) * inv, from_fx(bv[u][1].y) * inv);
             }
-            *reinterpret_cast<uint2 *>(fr + (kb0 + u) * 2048) = make_uint2(pack_f16(h[0], h[1]), pack_f16(h[2], h[3]));
+            const uint32_t w0 = pack_f16(h[0], h[1]), w1 = pack_f16(h[2], h[3]);
+            bad |= f16x2_bad(w0) | f16x2_bad(w1);
+            *reinterpret_cast<uint2 *>(fr + (kb0 + u) * 2048) = make_uint2(w0, w1);
         }
     }
+    if (bad) range_err(310);
 }
 
 
@@ -1205,6 +1258,7 @@ __device__ __noinline__ uint32_t cons_gemv(int st, const DLayer *Lp, const Route
             }
         }
         const int slot = ci % MK_RING;
+        if (k == 0) mark(c, st * 16 + 7);
         unsigned long long cy1 = prof ? clock64() : 0;
         if (mbar_wait(&full[slot], (ci / MK_RING) & 1, c, 200 + st)) {
             unsigned long long cy2 = prof ? clock64() : 0;
@@ -1968,6 +2022,50 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     return ci;
 }
 
+// ------------------------------------------------------------------ L2 prefetch
+// The weights of the dense stages and the KV pages of a layer do not depend on
+// the step's data, so they are requested into L2 ahead of use, while the
+// latency-bound stages leave HBM mostly idle; the producer's later tile copies
+// then hit L2.  Tile k of this CTA's share of stage st is requested by lane 0
+// of consumer warp k % 8.
+__device__ __noinline__ void l2_prefetch_stage(int st, const DLayer *Lp, const RouteSm *rt) {
+    const Ctx c = make_ctx();
+    StageIter it;
+    stage_iter(it, c, st, *Lp, rt);
+    const int n = it.n;
+    for (int k = 0; k < n; ++k, it.advance()) {
+        if ((k & (MK_NCWARPS - 1)) != c.warp || c.lane != 0) continue;
+        const MatR &d = it.cur();
+        const int e = it.expert(), x = it.kc * d.xstep, y = it.rg * 256;
+        if (d.is3d) pf_l2_3d(d.tmap, x, y, e);
+        else pf_l2_2d(d.tmap, x, y);
+        if (d.dtype == MK_DT_FP8E4M3_B128)
+            pf_l2_bulk(d.scale + (long long)e * d.sest + (long long)it.kc * d.rows + y, min(256, d.rows - y) * 4);
+    }
+}
+// this CTA's KV pages of layer l (its attention split), K and V
+__device__ __noinline__ void l2_prefetch_kv(int l) {
+    const Ctx c = make_ctx();
+    const DModel &m = *c.m;
+    const AttUnit u = att_unit(c);
+    if (!u.active) return;
+    const int nbox = (m.d * m.kv_es) / 128;
+    const CUtensorMap *km = c.p->kvmaps + 2 * l, *vm = km + 1;
+    for (int j = u.p0 + c.warp; j < u.pc1; j += MK_NCWARPS) {
+        if (c.lane >= 2 * nbox) continue;
+        const int phys = __ldg(c.p->page_table + j);
+        const int y = (phys * m.Hkv + u.g) * m.P, bx = c.lane >> 1;
+        pf_l2_2d((c.lane & 1) ? vm : km, bx * (128 / m.kv_es), y);
+    }
+}
+__device__ void l2_prefetch_layer(const DLayer *Lp, const RouteSm *rt, int l, bool with_qkv) {
+    if (with_qkv) l2_prefetch_stage(ST_QKV, Lp, rt);
+    l2_prefetch_stage(ST_O, Lp, rt);
+    l2_prefetch_stage(ST_ROUTER, Lp, rt);
+    if (make_ctx().m->nshared) l2_prefetch_stage(ST_SHA, Lp, rt);
+    l2_prefetch_kv(l);
+}
+
 // ------------------------------------------------------------------ consumer
 // copy one layer's descriptors into shared memory (consumer threads)
 __device__ __noinline__ void copy_layer_nc(DLayer *dst, const DLayer *src) {
@@ -2004,9 +2102,11 @@ __device__ __noinline__ void consumer() {
             int t = (int)(i / m.H), col = (int)(i - (long long)t * m.H);
             float v = p.mode ? __ldg(p.hidden_in + i)
                              : bf16_to_f(__ldg(m.embed + (long long)__ldg(p.tokens + t) * m.H + col));
+            if (fx_bad(v)) range_err(330);
             __stcg(m.res + (long long)t * m.H + col, to_fx(v));
         }
     }
+    if (MK_L2PF && !f32path) l2_prefetch_layer(&c.misc->L[0], &c.rt[0], p.mode ? p.layer : 0, false);
     if (!grid_sync(c, 1)) return;
     for (int li = 0; li < nl; ++li) {
         const int l = p.mode ? p.layer : li;
@@ -2014,6 +2114,7 @@ __device__ __noinline__ void consumer() {
         RouteSm *rt = &c.rt[li & 1];
         // ---- QKV
         {
+            mark(c, ST_QKV * 16 + 5);
             ActSrc a{m.res, nullptr, m.H, L.attn_norm};
             int b, e;
             split_range(stage_total(m, ST_QKV, L, rt), c.G, c.cta, b, e);
@@ -2026,6 +2127,7 @@ __device__ __noinline__ void consumer() {
                 const int nkc = L.qkv.n_kc;
                 build_frags(a, needed_kb(b, e, L.qkv), b < nkc ? needed_kb(b, min(e, nkc), L.qkv) : 0u, 0);
             }
+            mark(c, ST_QKV * 16 + 6);
             zero_slice(c, m.sh_acc, (long long)MK_MAXT * 2 * m.I);
             zero_slice(c, m.ea_acc, (long long)MK_MAXT * m.K * 2 * m.I);
             bar_consumers();
@@ -2042,11 +2144,20 @@ __device__ __noinline__ void consumer() {
         if (!grid_sync(c, 3)) return;
         // ---- O projection (+ residual)
         {
+            mark(c, ST_O * 16 + 5);
+            if (MK_L2PF && !f32path && p.mode == 0 && li + 1 < nl) {
+                // the next layer's descriptors (the producer reads them only
+                // after this layer's routing, published after this copy)
+                copy_layer(c, &c.misc->L[(li + 1) & 1], m.layers + li + 1);
+                bar_consumers();
+                l2_prefetch_layer(&c.misc->L[(li + 1) & 1], &c.rt[(li + 1) & 1], li + 1, true);
+            }
             ActSrc a{nullptr, m.o_buf, m.Hq * m.d, nullptr};
             int b, e;
             split_range(stage_total(m, ST_O, L, rt), c.G, c.cta, b, e);
             if (f32path) build_act32(a, m.Hq * m.d);
             else build_frags(a, needed_kb(b, e, L.o));
+            mark(c, ST_O * 16 + 6);
             zero_slice(c, m.qkv_acc, (long long)MK_MAXT * m.nqkv);
             bar_consumers();
             mark(c, ST_O * 16 + 0);
@@ -2063,6 +2174,7 @@ __device__ __noinline__ void consumer() {
             } else {
                 build_frags(a, chunk_kb_mask(c, m.H), ssq_owner_mask(c, m.H), 1);
             }
+            mark(c, ST_ROUTER * 16 + 6);
             bar_consumers();
             mark(c, ST_ROUTER * 16 + 0);
             ci = cons_gemv(ST_ROUTER, &(L), rt, ci);
@@ -2071,7 +2183,8 @@ __device__ __noinline__ void consumer() {
             // descriptors of the next layer, copied while the barrier settles.
             // The producer reads them only after this layer's routing, which
             // these threads publish after the copy.
-            if (p.mode == 0 && li + 1 < nl) copy_layer(c, &c.misc->L[(li + 1) & 1], m.layers + li + 1);
+            if (!(MK_L2PF && !f32path) && p.mode == 0 && li + 1 < nl)
+                copy_layer(c, &c.misc->L[(li + 1) & 1], m.layers + li + 1);
             if (!grid_wait(c, 5)) return;
             mark(c, ST_EXPA * 16 + 3);
             route_layer(&L, rt);
@@ -2084,9 +2197,11 @@ __device__ __noinline__ void consumer() {
                         if (p.out_idx) p.out_idx[i] = rt->idx[i / m.K][i % m.K];
                         if (p.out_w) p.out_w[i] = rt->w[i / m.K][i % m.K];
                     }
-                } else if (p.trace) {
-                    for (int i = c.tid; i < c.T * m.K; i += MK_NCWARPS * 32)
-                        p.trace[(long long)l * c.T * m.K + i] = rt->idx[i / m.K][i % m.K];
+                } else {
+                    for (int i = c.tid; i < c.T * m.K; i += MK_NCWARPS * 32) {
+                        if (p.trace) p.trace[(long long)l * c.T * m.K + i] = rt->idx[i / m.K][i % m.K];
+                        if (p.wtrace) p.wtrace[(long long)l * c.T * m.K + i] = rt->w[i / m.K][i % m.K];
+                    }
                 }
             }
             ci = cons_gemv(ST_EXPA, &(L), rt, ci);
@@ -2262,6 +2377,9 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_step_kernel(const __grid_con
         int ok = (*(volatile int *)&ctrl->abort == 0) ? 1 : 0;
         for (int t = 0; t < p.T; ++t)
             if (__ldg(p.positions + t) != ctx + t) ok = 0;
+        // entry points that stage per-position tables on the host (the RoPE rows
+        // of the allocation-free layer call) pass the ctx they staged for
+        if (p.host_ctx1 != 0 && ctx != p.host_ctx1 - 1) ok = 0;
         if (ctx < 0 || (long long)ctx + p.T > (long long)gm->max_pages * P) ok = 0;
         if (ok) {
             int np = (ctx + p.T + P - 1) / P;

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmk.so")
 
 MK_OK, MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_NOMEM = 0, -1, -2, -3
-MK_ERR_TIMEOUT, MK_ERR_CUDA, MK_ERR_BAD_STATE, MK_ERR_BAD_INPUT = -4, -5, -6, -7
+MK_ERR_TIMEOUT, MK_ERR_CUDA, MK_ERR_BAD_STATE, MK_ERR_BAD_INPUT, MK_ERR_RANGE = -4, -5, -6, -7, -8
 MK_DT_F32, MK_DT_BF16, MK_DT_FP8E4M3_B128 = 0, 1, 2
 MK_DESC_VERSION = 1
 
@@ -98,7 +98,7 @@ def lib() -> ctypes.CDLL:
                                            ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
                                            _vp, _vp, _vp, _vp]
     L.mk_layer_forward_noalloc.restype = S
-    L.mk_set_routing_trace.argtypes = [_vp, _vp]
+    L.mk_set_routing_trace.argtypes = [_vp, _vp, _vp]
     L.mk_set_routing_trace.restype = S
     L.mk_set_stage_trace.argtypes = [_vp, _vp, ctypes.c_int, _vp]
     L.mk_set_stage_trace.restype = S
@@ -201,8 +201,8 @@ def mk_layer_forward_noalloc(desc: mk_model_desc, lw: mk_layer_weights, k_pool, 
     return _check(None, s) if check else s
 
 
-def mk_set_routing_trace(st, trace) -> int:
-    return _check(st, lib().mk_set_routing_trace(st, _ptr(trace)))
+def mk_set_routing_trace(st, idx_trace, w_trace=None) -> int:
+    return _check(st, lib().mk_set_routing_trace(st, _ptr(idx_trace), _ptr(w_trace)))
 
 
 def mk_set_stage_trace(st, times, capacity=0, events=None) -> int:

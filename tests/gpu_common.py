@@ -9,6 +9,11 @@ from tests import helpers
 
 GAP = 1e-3            # decisive routing / argmax gap
 TOL = {synth.WDT_F32: 1e-4, synth.WDT_BF16: 2e-2, synth.WDT_FP8: 6e-2}
+# routing weights where the selection is decisive: the kernel forms them in
+# fp32 from the same sigmoid scores, so they follow the oracle far more closely
+# than the hidden state does (a router normalising the biased keys s + b
+# instead of s would move each weight by about 1e-2)
+WTOL = {synth.WDT_F32: 1e-5, synth.WDT_BF16: 1e-3, synth.WDT_FP8: 1e-3}
 
 
 class Built:
@@ -53,12 +58,14 @@ class Built:
         if trace:
             tr = torch.full((self.cfg.n_layers, T, self.cfg.top_k), -1, dtype=torch.int32,
                             device="cuda")
-            mk.mk_set_routing_trace(self.st, tr)
+            self.wtrace = torch.full((self.cfg.n_layers, T, self.cfg.top_k), float("nan"),
+                                     dtype=torch.float32, device="cuda")
+            mk.mk_set_routing_trace(self.st, tr, self.wtrace)
         mk.mk_decode_step(self.st, tok, T, self.positions(T), self.kvargs.kv, logits, acc, am)
         st = mk.mk_get_status(self.st)
         assert st == mk.MK_OK, mk.mk_last_error(self.st)
         if trace:
-            mk.mk_set_routing_trace(self.st, None)
+            mk.mk_set_routing_trace(self.st, None, None)
         return logits, int(acc.item()), am, tr
 
 
@@ -114,3 +121,21 @@ def check_routing(info, gpu_idx, K, where=""):
             assert g == o, "%s token %d: gpu %s oracle %s" % (where, t, sorted(g), sorted(o))
         else:
             assert valid_choice(info["key"][t], list(g), K), "%s token %d invalid tie choice" % (where, t)
+
+
+def check_weights(info, gpu_idx, gpu_w, wtol, where=""):
+    """Routing weights of every token whose GPU selection equals the oracle's (all
+    decisive tokens, and near ties where the oracle took the GPU's choice): each
+    expert's weight within wtol of the oracle's.  Returns the largest difference."""
+    worst = 0.0
+    for t in range(gpu_idx.shape[0]):
+        o = {int(e): float(info["w"][t, j]) for j, e in enumerate(info["idx"][t])}
+        g = [int(e) for e in gpu_idx[t]]
+        if set(g) != set(o):
+            continue
+        for j, e in enumerate(g):
+            d = abs(float(gpu_w[t, j]) - o[e])
+            worst = max(worst, d)
+            assert d <= wtol, "%s token %d expert %d: gpu w %.6f oracle %.6f" % (
+                where, t, e, float(gpu_w[t, j]), o[e])
+    return worst

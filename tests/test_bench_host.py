@@ -50,3 +50,21 @@ def test_workload_string_follows_the_run():
     assert bench.workload_of(synth.stack_config()) == bench.WORKLOAD
     w = bench.workload_of(synth.stack_config(n_layers=2, T=4))
     assert w.startswith("2-layer") and "T=4 (k=3 drafts" in w and w != bench.WORKLOAD
+
+
+def test_planned_tokens_per_step_follow_the_draws():
+    # a block accepts the run of leading agreements of its draws; at 0.83 the
+    # mean approaches the expectation sum_j 0.83^j = 3.96 tokens per step
+    plan = bench.draft_plan(32, 5, 129280, seed=3)
+    acc = bench.planned_accepts(plan)
+    for (_, agree, _), n in zip(plan, acc):
+        assert all(agree[:n]) and (n == 5 or not agree[n])
+    tps = bench.tokens_per_step_of(plan, 32)
+    assert abs(tps - (sum(acc) / 32 + 1)) < 1e-12
+    assert 3.0 < tps < 5.0
+    # cycling: 40 steps over 32 blocks count the first 8 twice
+    assert abs(bench.tokens_per_step_of(plan, 40) - ((sum(acc) + sum(acc[:8])) / 40 + 1)) < 1e-12
+    # the same seed gives the same plan in both arms
+    assert bench.draft_plan(32, 5, 129280, seed=3) == plan
+    big = bench.draft_plan(bench.DRAFT_BLOCKS, 5, 129280, seed=3)
+    assert abs(bench.tokens_per_step_of(big) - 3.96) < 0.15

@@ -24,13 +24,8 @@ def _run(cfg, ctxs=None, T=None, x_seed=11, l=0):
         ref, info = gc.oracle_layer(b, x.cpu().numpy(), l, gpu_idx=idx.cpu().numpy(), log=log)
         gc.check_routing(info, idx.cpu().numpy(), cfg.top_k)
         err = helpers.rel_err(out.cpu().numpy(), ref)
-        # routing weights of the GPU's selection
-        wg = w.cpu().numpy()
-        for t in range(T):
-            o = {int(e): info["w"][t, j] for j, e in enumerate(info["idx"][t])}
-            for j, e in enumerate(idx[t].tolist()):
-                if e in o:
-                    assert abs(wg[t, j] - o[e]) < 5 * gc.TOL[cfg.weight_dtype] + 1e-5
+        # routing weights of the GPU's selection, where it equals the oracle's
+        gc.check_weights(info, idx.cpu().numpy(), w.cpu().numpy(), gc.WTOL[cfg.weight_dtype])
         # K/V appended at positions ctx..ctx+T-1 (stored in the cache dtype)
         kv_err = _appended_err(b, info, l, T)
         return err, kv_err, log, info
@@ -98,5 +93,27 @@ def test_fp8_layer_is_deterministic():
         x = torch.randn((cfg.T, cfg.hidden), generator=torch.Generator().manual_seed(3)).cuda()
         outs = [b.layer(x)[0].clone() for _ in range(2)]
         assert torch.equal(outs[0], outs[1])
+    finally:
+        b.close()
+
+
+def test_out_of_range_input_is_reported():
+    """A residual entry of 1e5 cannot be an f16 GEMV input (largest finite value
+    65504): the layer must stop with MK_ERR_RANGE rather than return infinities;
+    after mk_reset the same state computes normal inputs again."""
+    cfg = synth.fp8_layer_config(ctx=100, T=2)
+    b = gc.Built(cfg)
+    try:
+        x = torch.randn((cfg.T, cfg.hidden), generator=torch.Generator().manual_seed(4)).cuda()
+        good, _, _ = b.layer(x)
+        good = good.clone()
+        y = x.clone()
+        y[1, 77] = 1e5
+        out = torch.empty_like(y)
+        mk.mk_layer_forward(b.st, 0, y, cfg.T, b.positions(cfg.T), b.kvargs.kv, out)
+        assert mk.mk_get_status(b.st) == mk.MK_ERR_RANGE
+        assert mk.mk_reset(b.st) == mk.MK_OK
+        again, _, _ = b.layer(x)
+        assert torch.equal(again, good)
     finally:
         b.close()

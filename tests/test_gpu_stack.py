@@ -45,8 +45,10 @@ def compare_step(b: gc.Built, toks):
                              b.model.final_norm.cpu().numpy().astype(np.float64),
                              helpers.lm_head_lin(b.model), dims, kvs, b.kv.ctx[0],
                              route_hook_factory=lambda l: gc.tie_hook(tr[l], cfg.top_k, log))
+    wt = b.wtrace.cpu().numpy()
     for l, info in enumerate(r["layers"]):
         gc.check_routing(info, tr[l], cfg.top_k, where="layer %d" % l)
+        gc.check_weights(info, tr[l], wt[l], gc.WTOL[cfg.weight_dtype], where="layer %d" % l)
     lg = logits.cpu().numpy()
     err = helpers.rel_err(lg, r["logits"])
     ref = r["logits"]
@@ -210,5 +212,68 @@ def test_timeout_is_reported_and_reset_recovers():
         assert mk.mk_reset(b.st) == mk.MK_OK
         again, acc2, _, _ = b.step(toks, trace=False)
         assert torch.equal(again, ref) and acc2 == acc_ref
+    finally:
+        b.close()
+
+
+def test_concurrency_streams_match_their_own_oracle_runs():
+    """The concurrency workload's shape at reduced depth: 4 streams, each with its
+    own context drawn from U[1024, 8192] (seed 4) and T = 6, over a 3-layer stack
+    of the full-width FP8 layer (hidden 4096, 384 experts top-8 + shared, vocab
+    129280), verified in one mk_decode_batch call.  Each stream is then run alone
+    with the routing trace on (its logits must equal the batch's bit for bit) and
+    compared with its own oracle run: routing and weights per layer, logits,
+    decisive argmax and the accept count."""
+    cfg = synth.stack_config(n_layers=3, seed=4)
+    ctxs = [int(c) for c in np.random.default_rng(4).integers(1024, 8193, 4)]
+    b = gc.Built(cfg, ctxs=ctxs)
+    try:
+        S, T, V, K = len(ctxs), cfg.T, cfg.vocab, cfg.top_k
+        toks = np.random.default_rng(44).integers(0, V, (S, T))
+        dims = helpers.oracle_dims(cfg)
+        layers = [helpers.layer_view(b.model, l) for l in range(cfg.n_layers)]
+        fn = b.model.final_norm.cpu().numpy().astype(np.float64)
+        lm = helpers.lm_head_lin(b.model)
+        # oracle inputs before the step appends K/V (positions >= ctx only)
+        kvs = [[helpers.kv_view(b.kv, l, stream=s) for l in range(cfg.n_layers)] for s in range(S)]
+        tok = torch.tensor(toks, dtype=torch.int32, device="cuda")
+        pos = torch.stack([torch.arange(c, c + T, dtype=torch.int32) for c in ctxs]).cuda()
+        logits = torch.empty((S, T, V), dtype=torch.float32, device="cuda")
+        acc = torch.zeros(S, dtype=torch.int32, device="cuda")
+        am = torch.zeros((S, T), dtype=torch.int32, device="cuda")
+        mk.mk_decode_batch(b.st, S, tok, T, pos, b.kvargs.kv, logits, acc, am)
+        assert mk.mk_get_status(b.st) == mk.MK_OK, mk.mk_last_error(b.st)
+        for s in range(S):
+            kv1 = mk.KVArgs(b.kv.k_pools, b.kv.v_pools, b.kv.page_table[s], b.kv.n_pages)
+            tr = torch.full((cfg.n_layers, T, K), -1, dtype=torch.int32, device="cuda")
+            wt = torch.zeros((cfg.n_layers, T, K), dtype=torch.float32, device="cuda")
+            lg1 = torch.empty((T, V), dtype=torch.float32, device="cuda")
+            a1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+            m1 = torch.zeros(T, dtype=torch.int32, device="cuda")
+            mk.mk_set_routing_trace(b.st, tr, wt)
+            mk.mk_decode_step(b.st, tok[s].contiguous(), T, pos[s].contiguous(), kv1.kv, lg1, a1, m1)
+            assert mk.mk_get_status(b.st) == mk.MK_OK, mk.mk_last_error(b.st)
+            mk.mk_set_routing_trace(b.st, None, None)
+            assert torch.equal(lg1, logits[s]) and int(a1) == int(acc[s]) and torch.equal(m1, am[s])
+            trn, wtn = tr.cpu().numpy(), wt.cpu().numpy()
+            log = []
+            r = oracle.stack_forward(toks[s].tolist(), helpers.embed_fn(b.model), layers, fn, lm,
+                                     dims, kvs[s], ctxs[s],
+                                     route_hook_factory=lambda l: gc.tie_hook(trn[l], K, log))
+            for l, info in enumerate(r["layers"]):
+                gc.check_routing(info, trn[l], K, where="stream %d layer %d" % (s, l))
+                gc.check_weights(info, trn[l], wtn[l], gc.WTOL[synth.WDT_FP8],
+                                 where="stream %d layer %d" % (s, l))
+            ref = r["logits"]
+            assert helpers.rel_err(logits[s].cpu().numpy(), ref) < gc.TOL[synth.WDT_FP8], s
+            rms = np.sqrt(np.mean(ref ** 2))
+            dec = []
+            for t in range(T):
+                srt = np.sort(ref[t])[::-1]
+                dec.append(srt[0] - srt[1] > gc.GAP * rms)
+                if dec[-1]:
+                    assert int(am[s, t]) == int(r["argmax"][t]), (s, t)
+            if all(dec):
+                assert int(acc[s]) == r["accepted"], s
     finally:
         b.close()
