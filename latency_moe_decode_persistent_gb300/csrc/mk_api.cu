@@ -329,19 +329,19 @@ mk_status mk_create(const mk_model_desc *desc, const mk_weights *w, mk_state **o
     if ((r = dalloc(st, &st->ctrl, sizeof(Ctrl))) != MK_OK) return bail(r);
     hm.ctrl = st->ctrl;
     if ((r = dalloc(st, &hm.att_cnt, sizeof(int) * L * Hkv)) != MK_OK) return bail(r);
-    if ((r = dalloc(st, &hm.qkv_acc, 8 * T8 * nqkv)) != MK_OK) return bail(r);
+    if ((r = dalloc(st, &hm.o_buf, 4 * T8 * Hq * hd)) != MK_OK) return bail(r);
+    if (cudaMemset(hm.att_cnt, 0, sizeof(int) * L * Hkv) != cudaSuccess) return bail(fail(st, MK_ERR_CUDA, "memset"));
+    if ((r = dalloc(st, &hm.qkv_acc, 2 * 8 * T8 * nqkv)) != MK_OK) return bail(r);
     if ((r = dalloc(st, &hm.res, 8 * T8 * H)) != MK_OK) return bail(r);
-    if ((r = dalloc(st, &hm.rlog, 8 * T8 * E)) != MK_OK) return bail(r);
-    if ((r = dalloc(st, &hm.sh_acc, 8 * T8 * 2 * I)) != MK_OK) return bail(r);
-    if ((r = dalloc(st, &hm.ea_acc, 8 * T8 * d.top_k * 2 * I)) != MK_OK) return bail(r);
+    if ((r = dalloc(st, &hm.rlog, 2 * 8 * T8 * E)) != MK_OK) return bail(r);
+    if ((r = dalloc(st, &hm.sh_acc, 2 * 8 * T8 * 2 * I)) != MK_OK) return bail(r);
+    if ((r = dalloc(st, &hm.ea_acc, 2 * 8 * T8 * d.top_k * 2 * I)) != MK_OK) return bail(r);
     if ((r = dalloc(st, &hm.logit_acc, 8 * T8 * (d.vocab > 0 ? d.vocab : 1))) != MK_OK) return bail(r);
     if ((r = dalloc(st, &hm.ssq, 4 * 3 * MK_MAXKB * T8)) != MK_OK) return bail(r);
-    if ((r = dalloc(st, &hm.o_buf, 4 * T8 * Hq * hd)) != MK_OK) return bail(r);
     if ((r = dalloc(st, &hm.att_part, 4ull * Hkv * MK_MAXSPLIT * MK_MAXROWS * (hd + 2))) != MK_OK) return bail(r);
     if ((r = dalloc(st, &hm.cand_v, 4 * T8 * st->grid)) != MK_OK) return bail(r);
     if ((r = dalloc(st, &hm.cand_i, 4 * T8 * st->grid)) != MK_OK) return bail(r);
     if (cudaMemset(st->ctrl, 0, sizeof(Ctrl)) != cudaSuccess) return bail(fail(st, MK_ERR_CUDA, "memset ctrl"));
-    if (cudaMemset(hm.att_cnt, 0, sizeof(int) * L * Hkv) != cudaSuccess) return bail(fail(st, MK_ERR_CUDA, "memset"));
     if ((r = dalloc(st, &st->d_model, sizeof(DModel))) != MK_OK) return bail(r);
     if (cudaMemcpy(st->d_model, &hm, sizeof(DModel), cudaMemcpyHostToDevice) != cudaSuccess)
         return bail(fail(st, MK_ERR_CUDA, "copy of model block"));
@@ -671,14 +671,14 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     const size_t o_rope = cv.take<float2>(T8 * (hd / 2) * sizeof(float2));
     const size_t o_ctrl = cv.take<Ctrl>(sizeof(Ctrl));
     const size_t o_attcnt = cv.take<int>(sizeof(int) * Hkv);
-    const size_t o_qkv = cv.take<long long>(8 * T8 * nqkv);
+    const size_t o_obuf = cv.take<float>(4 * T8 * Hq * hd);
+    const size_t o_qkv = cv.take<long long>(2 * 8 * T8 * nqkv);
     const size_t o_res = cv.take<long long>(8 * T8 * H);
-    const size_t o_rlog = cv.take<long long>(8 * T8 * E);
-    const size_t o_sh = cv.take<long long>(8 * T8 * 2 * I);
-    const size_t o_ea = cv.take<long long>(8 * T8 * d.top_k * 2 * I);
+    const size_t o_rlog = cv.take<long long>(2 * 8 * T8 * E);
+    const size_t o_sh = cv.take<long long>(2 * 8 * T8 * 2 * I);
+    const size_t o_ea = cv.take<long long>(2 * 8 * T8 * d.top_k * 2 * I);
     const size_t o_logit = cv.take<long long>(8 * T8);
     const size_t o_ssq = cv.take<float>(4 * 3 * MK_MAXKB * T8);
-    const size_t o_obuf = cv.take<float>(4 * T8 * Hq * hd);
     const size_t o_part = cv.take<float>(4ull * Hkv * MK_MAXSPLIT * MK_MAXROWS * (hd + 2));
     const size_t o_candv = cv.take<float>(4 * T8 * nd->grid);
     const size_t o_candi = cv.take<int>(4 * T8 * nd->grid);
@@ -753,6 +753,7 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     hm.rope = reinterpret_cast<const float2 *>(base + o_rope) - (long long)ctx * (hd / 2);
     hm.ctrl = reinterpret_cast<Ctrl *>(base + o_ctrl);
     hm.att_cnt = reinterpret_cast<int *>(base + o_attcnt);
+    hm.o_buf = reinterpret_cast<float *>(base + o_obuf);
     hm.qkv_acc = reinterpret_cast<long long *>(base + o_qkv);
     hm.res = reinterpret_cast<long long *>(base + o_res);
     hm.rlog = reinterpret_cast<long long *>(base + o_rlog);
@@ -760,7 +761,6 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     hm.ea_acc = reinterpret_cast<long long *>(base + o_ea);
     hm.logit_acc = reinterpret_cast<long long *>(base + o_logit);
     hm.ssq = reinterpret_cast<float *>(base + o_ssq);
-    hm.o_buf = reinterpret_cast<float *>(base + o_obuf);
     hm.att_part = reinterpret_cast<float *>(base + o_part);
     hm.cand_v = reinterpret_cast<float *>(base + o_candv);
     hm.cand_i = reinterpret_cast<int *>(base + o_candi);

@@ -84,15 +84,16 @@ struct DModel {
     // workspace
     Ctrl *ctrl;
     int *att_cnt;                      // [L][Hkv]
-    long long *qkv_acc;                // [MAXT][nqkv]
+    // per-layer accumulators: two copies each, selected by the layer's parity
+    long long *qkv_acc;                // [2][MAXT][nqkv]
     long long *res;                    // [MAXT][H]   residual stream
-    long long *rlog;                   // [MAXT][E]   router logits (un-normalised)
-    long long *sh_acc;                 // [MAXT][2][I] shared expert gate/up
-    long long *ea_acc;                 // [MAXT][K][2][I] routed expert gate/up
+    long long *rlog;                   // [2][MAXT][E]   router logits (un-normalised)
+    long long *sh_acc;                 // [2][MAXT][2][I] shared expert gate/up
+    long long *ea_acc;                 // [2][MAXT][K][2][I] routed expert gate/up
     long long *logit_acc;              // [MAXT][V]
     float *ssq;                        // [3][MAXKB][MAXT] sum-of-squares partials
     float *o_buf;                      // [MAXT][Hq*d] attention output
-    float *att_part;                   // [Hkv][MAXSPLIT][MAXROWS][d+2]
+    float *att_part;                   // [Hkv][MAXSPLIT][MAXROWS][d+2] attention split partials
     float *cand_v;                     // [G][MAXT] argmax candidates
     int *cand_i;
 };

@@ -45,12 +45,6 @@
 #define MK_F32_MODEL 0
 #endif
 
-// MK_L2PF 1: request the next layer's dense weights and KV pages into L2
-// during the current layer's O projection
-#ifndef MK_L2PF
-#define MK_L2PF 0
-#endif
-
 namespace {
 
 constexpr bool kF32 = MK_F32_MODEL != 0;
@@ -139,20 +133,6 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
             "r"(sa(dst)),
         "l"(src), "r"(bytes), "r"(sa(bar))
         : "memory");
-}
-// L2 prefetches (no shared memory, no completion): a box of a tensor map, or
-// a contiguous range (16-byte aligned, a multiple of 16 bytes)
-__device__ __forceinline__ void pf_l2_2d(const CUtensorMap *map, int x, int y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
-                 : "memory");
-}
-__device__ __forceinline__ void pf_l2_3d(const CUtensorMap *map, int x, int y, int z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x), "r"(y),
-                 "r"(z)
-                 : "memory");
-}
-__device__ __forceinline__ void pf_l2_bulk(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void bar_consumers() {
     asm volatile("bar.sync 1, %0;" ::"n"(MK_NCWARPS * 32) : "memory");
@@ -288,10 +268,13 @@ struct MiscSm {
     int valid, ctx, nsplit;
     int nbar;                    // grid barriers passed (thread 0)
     int nmark;                   // trace events written (thread 0)
+    int par;                     // parity of the current layer: selects its accumulators
     unsigned long long base;     // barrier counter at launch
-    const Params *p;
+    const Params *p;             // points at pc below
     DModel m;
     DLayer L[2];                 // descriptors of layers with parity 0 / 1
+    Params pc;                   // the launch parameters: generic loads from the
+                                 // kernel's parameter space are slow, shared memory is not
 };
 
 struct Ctx {
@@ -511,9 +494,24 @@ __device__ __forceinline__ bool grid_sync(const Ctx &c, int where) {
 }
 
 // ------------------------------------------------------------------ schedules
+// the products stay below 2^32 for every split this kernel makes (at most
+// 8 x 129,280 elements over 152 parts), so 32-bit unsigned arithmetic is exact
 __device__ __forceinline__ void split_range(int total, int parts, int part, int &b, int &e) {
-    b = (int)((long long)total * part / parts);
-    e = (int)((long long)total * (part + 1) / parts);
+    b = (int)((unsigned)total * (unsigned)part / (unsigned)parts);
+    e = (int)((unsigned)total * (unsigned)(part + 1) / (unsigned)parts);
+}
+
+// Per-layer accumulators come in two copies selected by the layer's parity, so
+// that the copy the next layer uses can be cleared while this layer runs.
+enum { ACC_QKV = 0, ACC_SH, ACC_EA, ACC_RLOG };
+__device__ __forceinline__ long long acc_elems(const DModel &m, int which) {
+    return which == ACC_QKV ? (long long)MK_MAXT * m.nqkv
+         : which == ACC_SH ? (long long)MK_MAXT * 2 * m.I
+         : which == ACC_EA ? (long long)MK_MAXT * m.K * 2 * m.I : (long long)MK_MAXT * m.E;
+}
+__device__ __forceinline__ long long *acc_ptr(const DModel &m, int which, int par) {
+    long long *b = which == ACC_QKV ? m.qkv_acc : which == ACC_SH ? m.sh_acc : which == ACC_EA ? m.ea_acc : m.rlog;
+    return b + (par ? acc_elems(m, which) : 0);
 }
 
 __device__ int stage_total(const DModel &m, int st, const DLayer &L, const RouteSm *rt) {
@@ -993,11 +991,11 @@ __device__ __forceinline__ Tgt make_tgt(const Ctx &c, int st, int ex, int mat, i
     g.row_limit = rows;
     g.K2I = m.K * 2 * m.I;
     switch (st) {
-        case ST_QKV: g.base = m.qkv_acc; g.tstride = m.nqkv; break;
+        case ST_QKV: g.base = acc_ptr(m, ACC_QKV, c.misc->par); g.tstride = m.nqkv; break;
         case ST_O: g.base = m.res; g.tstride = m.H; break;
-        case ST_ROUTER: g.base = m.rlog; g.tstride = m.E; break;
-        case ST_SHA: g.base = m.sh_acc + mat * m.I; g.tstride = 2 * m.I; break;
-        case ST_EXPA: g.base = m.ea_acc + mat * m.I; g.tstride = 2 * m.I; break;
+        case ST_ROUTER: g.base = acc_ptr(m, ACC_RLOG, c.misc->par); g.tstride = m.E; break;
+        case ST_SHA: g.base = acc_ptr(m, ACC_SH, c.misc->par) + mat * m.I; g.tstride = 2 * m.I; break;
+        case ST_EXPA: g.base = acc_ptr(m, ACC_EA, c.misc->par) + mat * m.I; g.tstride = 2 * m.I; break;
         case ST_EXPB: g.base = m.res; g.tstride = m.H; break;
         default: g.base = m.logit_acc; g.tstride = m.V; break;
     }
@@ -1161,9 +1159,9 @@ __device__ __noinline__ void build_h_frags(const RouteSm *rt, int ex, bool f32pa
     const bool shared = ex >= rt->nd;
     auto base = [&](int t) -> const long long * {
         if (t >= c.T) return nullptr;
-        if (shared) return m.sh_acc + (long long)t * 2 * m.I;
+        if (shared) return acc_ptr(m, ACC_SH, c.misc->par) + (long long)t * 2 * m.I;
         int j = rt->dslot[ex][t];
-        return j < 0 ? nullptr : m.ea_acc + (long long)(t * m.K + j) * 2 * m.I;
+        return j < 0 ? nullptr : acc_ptr(m, ACC_EA, c.misc->par) + (long long)(t * m.K + j) * 2 * m.I;
     };
     if (f32path) {
         float *dst = reinterpret_cast<float *>(c.sm + SM_SCRATCH);
@@ -1291,8 +1289,14 @@ __device__ __noinline__ uint32_t cons_gemv(int st, const DLayer *Lp, const Route
 // ------------------------------------------------------------------ small helpers
 __device__ __noinline__ void zero_slice_nc(long long *p, long long n) {
     const Ctx c = make_ctx();
-    long long b = n * c.cta / c.G, e = n * (c.cta + 1) / c.G;
-    for (long long i = b + c.tid; i < e; i += MK_NCWARPS * 32) __stcg(p + i, 0ll);
+    int b, e;
+    split_range((int)n, c.G, c.cta, b, e);
+    for (int i = b + c.tid; i < e; i += MK_NCWARPS * 32) __stcg(p + i, 0ll);
+}
+// this CTA's share of clearing the accumulators of parity par
+__device__ __noinline__ void zero_accs(int par) {
+    const Ctx c = make_ctx();
+    for (int w = ACC_QKV; w <= ACC_RLOG; ++w) zero_slice_nc(acc_ptr(*c.m, w, par), acc_elems(*c.m, w));
 }
 __device__ __forceinline__ void zero_slice(const Ctx &c, long long *p, long long n) {
     (void)c;
@@ -1395,7 +1399,7 @@ __device__ __noinline__ void route_layer(const DLayer *Lp, RouteSm *rt) {
             raw[i] = 0;
             bias[i] = 0.f;
             if (e < m.E) {
-                raw[i] = __ldcg(m.rlog + (long long)t * m.E + e);
+                raw[i] = __ldcg(acc_ptr(m, ACC_RLOG, c.misc->par) + (long long)t * m.E + e);
                 bias[i] = __ldg(L.router_bias + e);
             }
         }
@@ -1490,7 +1494,8 @@ __device__ __noinline__ void route_layer(const DLayer *Lp, RouteSm *rt) {
 // ------------------------------------------------------------------ attention
 // q rows are ordered (t, head-in-group): row = t * G + hh
 __device__ float qkv_val(const Ctx &c, int t, int col) {
-    return from_fx(__ldcg(c.m->qkv_acc + (long long)t * c.m->nqkv + col)) * c.misc->inv_rms[0][t];
+    return from_fx(__ldcg(acc_ptr(*c.m, ACC_QKV, c.misc->par) + (long long)t * c.m->nqkv + col)) *
+           c.misc->inv_rms[0][t];
 }
 
 // prepares rotated q (scratch) and, for the unit holding the new block, the
@@ -1499,18 +1504,19 @@ __device__ void att_prepare(const Ctx &c, int l, const AttUnit &u, bool mma_path
     const DModel &m = *c.m;
     const int G = m.Hq / m.Hkv, R = G * c.T, hd = m.d / 2;
     unsigned char *scr = c.sm + SM_SCRATCH;
-    // rotated queries: 4 consecutive pairs per item, loads of 4 items in flight
+    const long long *qkv = acc_ptr(m, ACC_QKV, c.misc->par);
+    // rotated queries: 4 consecutive pairs per item, two items per thread and batch
     const int nk4 = hd / 4, nitem = R * nk4;
-    for (int i0 = c.tid; i0 < nitem; i0 += 2 * MK_NCWARPS * 32) {
-        longlong2 xa[2][2], xb[2][2];
-        float4 ra[2][2];
+    longlong2 xa[2][2], xb[2][2];
+    float4 ra[2][2];
+    auto load = [&](int i0) {
 #pragma unroll
         for (int u4 = 0; u4 < 2; ++u4) {
             int i = i0 + u4 * MK_NCWARPS * 32;
             if (i < nitem) {
                 int row = i / nk4, k = (i - row * nk4) * 4;
                 int t = row / G, h = u.g * G + (row - t * G);
-                const long long *b = m.qkv_acc + (long long)t * m.nqkv + h * m.d + k;
+                const long long *b = qkv + (long long)t * m.nqkv + h * m.d + k;
                 xa[u4][0] = __ldcg(reinterpret_cast<const longlong2 *>(b));
                 xa[u4][1] = __ldcg(reinterpret_cast<const longlong2 *>(b) + 1);
                 xb[u4][0] = __ldcg(reinterpret_cast<const longlong2 *>(b + hd));
@@ -1520,6 +1526,20 @@ __device__ void att_prepare(const Ctx &c, int l, const AttUnit &u, bool mma_path
                 ra[u4][1] = __ldg(rp + 1);
             }
         }
+    };
+    // the first batch of query loads and the attention RMSNorm factors (warp t
+    // reduces token t's 128-column sum-of-squares partials) are in flight together
+    load(c.tid);
+    if (c.warp < c.T) {
+        const int t = c.warp;
+        float v = c.lane < m.H / 128 ? __ldcg(m.ssq + c.lane * MK_MAXT + t) : 0.f;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (c.lane == 0) c.misc->inv_rms[0][t] = rsqrtf(v / (float)m.H + m.eps);
+    }
+    bar_consumers();
+    for (int i0 = c.tid; i0 < nitem; i0 += 2 * MK_NCWARPS * 32) {
+        if (i0 != c.tid) load(i0);
 #pragma unroll
         for (int u4 = 0; u4 < 2; ++u4) {
             int i = i0 + u4 * MK_NCWARPS * 32;
@@ -1784,8 +1804,6 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     constexpr bool mma_path = !kF32;
     const int nbox = (m.d * m.kv_es) / 128, bs = m.P * 128;
     const int D2 = m.d + 2;
-    compute_inv_rms(c, 0);
-    bar_consumers();
     if (u.active) att_prepare(c, l, u, mma_path);
     bar_consumers();
     mark(c, ST_ATT * 16 + 0);
@@ -2022,50 +2040,6 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     return ci;
 }
 
-// ------------------------------------------------------------------ L2 prefetch
-// The weights of the dense stages and the KV pages of a layer do not depend on
-// the step's data, so they are requested into L2 ahead of use, while the
-// latency-bound stages leave HBM mostly idle; the producer's later tile copies
-// then hit L2.  Tile k of this CTA's share of stage st is requested by lane 0
-// of consumer warp k % 8.
-__device__ __noinline__ void l2_prefetch_stage(int st, const DLayer *Lp, const RouteSm *rt) {
-    const Ctx c = make_ctx();
-    StageIter it;
-    stage_iter(it, c, st, *Lp, rt);
-    const int n = it.n;
-    for (int k = 0; k < n; ++k, it.advance()) {
-        if ((k & (MK_NCWARPS - 1)) != c.warp || c.lane != 0) continue;
-        const MatR &d = it.cur();
-        const int e = it.expert(), x = it.kc * d.xstep, y = it.rg * 256;
-        if (d.is3d) pf_l2_3d(d.tmap, x, y, e);
-        else pf_l2_2d(d.tmap, x, y);
-        if (d.dtype == MK_DT_FP8E4M3_B128)
-            pf_l2_bulk(d.scale + (long long)e * d.sest + (long long)it.kc * d.rows + y, min(256, d.rows - y) * 4);
-    }
-}
-// this CTA's KV pages of layer l (its attention split), K and V
-__device__ __noinline__ void l2_prefetch_kv(int l) {
-    const Ctx c = make_ctx();
-    const DModel &m = *c.m;
-    const AttUnit u = att_unit(c);
-    if (!u.active) return;
-    const int nbox = (m.d * m.kv_es) / 128;
-    const CUtensorMap *km = c.p->kvmaps + 2 * l, *vm = km + 1;
-    for (int j = u.p0 + c.warp; j < u.pc1; j += MK_NCWARPS) {
-        if (c.lane >= 2 * nbox) continue;
-        const int phys = __ldg(c.p->page_table + j);
-        const int y = (phys * m.Hkv + u.g) * m.P, bx = c.lane >> 1;
-        pf_l2_2d((c.lane & 1) ? vm : km, bx * (128 / m.kv_es), y);
-    }
-}
-__device__ void l2_prefetch_layer(const DLayer *Lp, const RouteSm *rt, int l, bool with_qkv) {
-    if (with_qkv) l2_prefetch_stage(ST_QKV, Lp, rt);
-    l2_prefetch_stage(ST_O, Lp, rt);
-    l2_prefetch_stage(ST_ROUTER, Lp, rt);
-    if (make_ctx().m->nshared) l2_prefetch_stage(ST_SHA, Lp, rt);
-    l2_prefetch_kv(l);
-}
-
 // ------------------------------------------------------------------ consumer
 // copy one layer's descriptors into shared memory (consumer threads)
 __device__ __noinline__ void copy_layer_nc(DLayer *dst, const DLayer *src) {
@@ -2088,10 +2062,9 @@ __device__ __noinline__ void consumer() {
     const uint32_t allH = 0xffffffffu >> (32 - m.H / 128);
     int nl = p.mode ? 1 : m.L;
     // zero the accumulators, load the residual stream
-    zero_slice(c, m.qkv_acc, (long long)MK_MAXT * m.nqkv);
-    zero_slice(c, m.sh_acc, (long long)MK_MAXT * 2 * m.I);
-    zero_slice(c, m.ea_acc, (long long)MK_MAXT * m.K * 2 * m.I);
-    zero_slice(c, m.rlog, (long long)MK_MAXT * m.E);
+    // the first layer's accumulators (parity 0); each layer clears the next
+    // layer's copy while it waits at the barrier that ends its QKV stage
+    zero_accs(0);
     if (p.mode == 0) zero_slice(c, m.logit_acc, (long long)c.T * m.V);
     if (c.cta == 0)
         for (int i = c.tid; i < m.L * m.Hkv; i += MK_NCWARPS * 32) __stcg(m.att_cnt + i, 0);
@@ -2106,12 +2079,12 @@ __device__ __noinline__ void consumer() {
             __stcg(m.res + (long long)t * m.H + col, to_fx(v));
         }
     }
-    if (MK_L2PF && !f32path) l2_prefetch_layer(&c.misc->L[0], &c.rt[0], p.mode ? p.layer : 0, false);
     if (!grid_sync(c, 1)) return;
     for (int li = 0; li < nl; ++li) {
         const int l = p.mode ? p.layer : li;
         const DLayer &L = c.misc->L[li & 1];
         RouteSm *rt = &c.rt[li & 1];
+        if (c.tid == 0) c.misc->par = li & 1;  // read after the CTA barriers below
         // ---- QKV
         {
             mark(c, ST_QKV * 16 + 5);
@@ -2128,12 +2101,14 @@ __device__ __noinline__ void consumer() {
                 build_frags(a, needed_kb(b, e, L.qkv), b < nkc ? needed_kb(b, min(e, nkc), L.qkv) : 0u, 0);
             }
             mark(c, ST_QKV * 16 + 6);
-            zero_slice(c, m.sh_acc, (long long)MK_MAXT * 2 * m.I);
-            zero_slice(c, m.ea_acc, (long long)MK_MAXT * m.K * 2 * m.I);
             bar_consumers();
             mark(c, ST_QKV * 16 + 0);
             ci = cons_gemv(ST_QKV, &(L), rt, ci);
-            if (!grid_sync(c, 2)) return;
+            grid_arrive(c);
+            // the next layer's accumulators: their copy was last read in the
+            // previous layer, which every CTA has left
+            zero_accs((li + 1) & 1);
+            if (!grid_wait(c, 2)) return;
         }
         // ---- attention
         {
@@ -2145,20 +2120,12 @@ __device__ __noinline__ void consumer() {
         // ---- O projection (+ residual)
         {
             mark(c, ST_O * 16 + 5);
-            if (MK_L2PF && !f32path && p.mode == 0 && li + 1 < nl) {
-                // the next layer's descriptors (the producer reads them only
-                // after this layer's routing, published after this copy)
-                copy_layer(c, &c.misc->L[(li + 1) & 1], m.layers + li + 1);
-                bar_consumers();
-                l2_prefetch_layer(&c.misc->L[(li + 1) & 1], &c.rt[(li + 1) & 1], li + 1, true);
-            }
             ActSrc a{nullptr, m.o_buf, m.Hq * m.d, nullptr};
             int b, e;
             split_range(stage_total(m, ST_O, L, rt), c.G, c.cta, b, e);
             if (f32path) build_act32(a, m.Hq * m.d);
             else build_frags(a, needed_kb(b, e, L.o));
             mark(c, ST_O * 16 + 6);
-            zero_slice(c, m.qkv_acc, (long long)MK_MAXT * m.nqkv);
             bar_consumers();
             mark(c, ST_O * 16 + 0);
             ci = cons_gemv(ST_O, &(L), rt, ci);
@@ -2183,8 +2150,7 @@ __device__ __noinline__ void consumer() {
             // descriptors of the next layer, copied while the barrier settles.
             // The producer reads them only after this layer's routing, which
             // these threads publish after the copy.
-            if (!(MK_L2PF && !f32path) && p.mode == 0 && li + 1 < nl)
-                copy_layer(c, &c.misc->L[(li + 1) & 1], m.layers + li + 1);
+            if (p.mode == 0 && li + 1 < nl) copy_layer(c, &c.misc->L[(li + 1) & 1], m.layers + li + 1);
             if (!grid_wait(c, 5)) return;
             mark(c, ST_EXPA * 16 + 3);
             route_layer(&L, rt);
@@ -2208,7 +2174,6 @@ __device__ __noinline__ void consumer() {
             if (!grid_sync(c, 6)) return;
         }
         // ---- routed + shared down projections (+ residual)
-        zero_slice(c, m.rlog, (long long)MK_MAXT * m.E);
         mark(c, ST_EXPB * 16 + 0);
         ci = cons_gemv(ST_EXPB, &(L), rt, ci);
         if (!grid_sync(c, 7)) return;
@@ -2345,8 +2310,11 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_step_kernel(const __grid_con
     unsigned char *smem = smem_base();
     MiscSm *misc = reinterpret_cast<MiscSm *>(smem + SM_MISC);
     const DModel *gm = p.m;
-    // model block and first layer's descriptors into shared memory
+    // launch parameters, model block and first layer's descriptors into shared memory
     {
+        const int np = (int)(sizeof(Params) / 4);
+        for (int i = threadIdx.x; i < np; i += blockDim.x)
+            reinterpret_cast<uint32_t *>(&misc->pc)[i] = reinterpret_cast<const uint32_t *>(&p)[i];
         const int nw = (int)(sizeof(DModel) / 4);
         for (int i = threadIdx.x; i < nw; i += blockDim.x)
             reinterpret_cast<uint32_t *>(&misc->m)[i] = __ldg(reinterpret_cast<const uint32_t *>(gm) + i);
@@ -2369,7 +2337,8 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_step_kernel(const __grid_con
         misc->distinct_total = 0;
         misc->nbar = 0;
         misc->nmark = 0;
-        misc->p = &p;
+        misc->par = 0;
+        misc->p = &misc->pc;
         Ctrl *ctrl = gm->ctrl;
         // validate the step's inputs (every CTA reaches the same verdict)
         const int P = gm->P;
