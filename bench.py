@@ -41,11 +41,34 @@ WORKLOAD = ("43-layer FP8 (e4m3, 1x128 scales) MoE stack: H 4096, 32 q / 4 kv he
 
 def workload_of(cfg):
     """The workload string of a run: the default one, or the same stack with the
-    layer count and block size the run overrode."""
+    layer count, block size or routed-expert format the run overrode."""
+    w = WORKLOAD
+    if getattr(cfg, "routed_dtype", cfg.weight_dtype) == 3:
+        w = w.replace("384 experts top-8", "384 MXFP4 experts (e2m1, 1x32 e8m0 scales) top-8")
+    if cfg.kv_dtype == 2:
+        w = w.replace("bf16 KV", "FP8 e4m3 KV (per-layer K/V scales %g/%g)" % tuple(cfg.kv_scales))
+    if cfg.ctx != 2048:
+        w = w.replace("ctx 2048", "ctx %d" % cfg.ctx)
     if cfg.n_layers == 43 and cfg.T == 6:
-        return WORKLOAD
-    return WORKLOAD.replace("43-layer", "%d-layer" % cfg.n_layers).replace(
+        return w
+    return w.replace("43-layer", "%d-layer" % cfg.n_layers).replace(
         "T=6 (k=5 drafts", "T=%d (k=%d drafts" % (cfg.T, cfg.T - 1))
+
+
+def variant_kw(args, synth):
+    """Config overrides of the routed-expert format, KV format and context."""
+    kw = {}
+    if args.experts == "mxfp4":
+        kw["expert_dtype"] = synth.WDT_MXFP4
+    if args.kv == "fp8":
+        kw["kv_dtype"] = synth.WDT_FP8
+        kw["kv_scales"] = FP8_KV_SCALES
+    if args.ctx:
+        kw["ctx"] = args.ctx
+    return kw
+
+
+FP8_KV_SCALES = (0.0125, 0.0125)   # value = code x scale: N(0, 1) entries span about +-400 codes
 
 
 def rank_info():
@@ -144,10 +167,14 @@ def algorithmic_bytes(cfg, distinct_per_step, ctx):
     H, I, E, d = cfg.hidden, cfg.expert_inter, cfg.n_experts, cfg.head_dim
     nqkv = cfg.qkv_rows
     fp8 = lambda rows, cols: rows * cols + (cols // 128) * rows * 4
-    expert = fp8(I, H) * 2 + fp8(H, I)
+    mxfp4 = lambda rows, cols: rows * cols // 2 + (cols // 32) * rows
+    shared = fp8(I, H) * 2 + fp8(H, I)
+    routed = shared if getattr(cfg, "routed_dtype", cfg.weight_dtype) != 3 else mxfp4(I, H) * 2 + mxfp4(H, I)
+    expert = routed
+    kv_es = 1 if cfg.kv_dtype == 2 else 2
     per_layer = (fp8(nqkv, H) + fp8(H, cfg.n_q_heads * d) + E * H * 2 + E * 4 + 2 * H * 4
-                 + (expert if cfg.n_shared else 0)
-                 + ctx * cfg.n_kv_heads * d * 2 * 2 + cfg.T * cfg.n_kv_heads * d * 2 * 2)
+                 + (shared if cfg.n_shared else 0)
+                 + ctx * cfg.n_kv_heads * d * 2 * kv_es + cfg.T * cfg.n_kv_heads * d * 2 * kv_es)
     total = cfg.n_layers * per_layer + distinct_per_step * expert
     total += cfg.T * H * 2 + H * 4 + cfg.vocab * H * 2 + cfg.T * cfg.vocab * 4
     return total
@@ -167,9 +194,10 @@ def oracle_sample(model, kv, cfg, toks, layers_to_time, ref_lm=True):
     for l in layers_to_time:
         lv = helpers.layer_view(model, l, expert_cache=cache)
         kc, vc = helpers.kv_view(kv, l)
-        oracle.layer_forward(x, lv, dims, kc, vc, kv.ctx[0])          # staging pass (untimed)
+        ksc = helpers.kv_scales(kv)[l]
+        oracle.layer_forward(x, lv, dims, kc, vc, kv.ctx[0], kv_scale=ksc)   # staging pass (untimed)
         t0 = time.perf_counter()
-        y, _ = oracle.layer_forward(x, lv, dims, kc, vc, kv.ctx[0])
+        y, _ = oracle.layer_forward(x, lv, dims, kc, vc, kv.ctx[0], kv_scale=ksc)
         per.append(time.perf_counter() - t0)
         x = y
     lm_s = 0.0
@@ -268,6 +296,7 @@ def run_mk(args):
         kw["n_layers"] = args.layers
     if args.T:
         kw["T"] = args.T
+    kw.update(variant_kw(args, synth))
     cfg = synth.stack_config(**kw)
     t_gen = time.perf_counter()
     model = synth.make_model(cfg, dev)
@@ -276,7 +305,7 @@ def run_mk(args):
     t_gen = time.perf_counter() - t_gen
     margs = mk.ModelArgs(model, cfg.T, kv.max_pages)
     st = mk.mk_create(margs.desc, margs.weights)
-    kva = mk.KVArgs(kv.k_pools, kv.v_pools, kv.page_table, kv.n_pages)
+    kva = mk.KVArgs(kv.k_pools, kv.v_pools, kv.page_table, kv.n_pages, kv.scales)
     T, V = cfg.T, cfg.vocab
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
@@ -398,7 +427,11 @@ def run_mk(args):
         "metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(slow_ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8e4m3 weights x f16 activations -> fp32 (bf16 LM head), int64 fixed-point reductions",
+        "dtype": (("fp8e4m3 weights x f16 activations -> fp32 (bf16 LM head), int64 fixed-point reductions"
+                   if args.experts == "fp8" else
+                   "mxfp4 routed experts, fp8e4m3 attention/shared weights x f16 activations -> fp32 "
+                   "(bf16 LM head), int64 fixed-point reductions")
+                  + ("; fp8e4m3 KV codes x f16 queries / probabilities" if args.kv == "fp8" else "")),
         "data": "synthetic (seeded random weights of the named architecture)",
         "config": {"workload": workload_of(cfg), "global_batch": world, "seq_len": T,
                    "parallelism": "replicas (1 stream per GPU)" if world > 1 else "single GPU",
@@ -607,12 +640,13 @@ def run_reference(args):
     import numpy as np
     import torch
     from latency_moe_decode_persistent_gb300 import synth
-    cfg = synth.stack_config()
+    vkw = variant_kw(args, synth)
+    cfg = synth.stack_config(**vkw)
     dev = torch.device("cuda", lrank) if torch.cuda.is_available() else torch.device("cpu")
     # only the layers the sample uses are generated (per-layer seeds make them
     # identical to the full model's)
     nl = min(cfg.n_layers, max(1, args.ref_layers))
-    sub = synth.stack_config(n_layers=nl)
+    sub = synth.stack_config(n_layers=nl, **vkw)
     model = synth.make_model(sub, dev)
     kv = synth.make_kv(sub, dev)
     plan = draft_plan(DRAFT_BLOCKS, cfg.T - 1, cfg.vocab, seed=3)
@@ -638,7 +672,7 @@ def run_reference(args):
         "full_step_ms_extrapolated": round(step_s * 1e3, 1),
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": cfg.T},
+        "config": {"workload": workload_of(cfg), "global_batch": 1, "seq_len": cfg.T},
         "tokens_per_step": round(tok_step, 4),
         "cpu_baseline": {"kind": "oracle", "cores": os.cpu_count(), "value": round(value, 6),
                          "sample": "each timed step (ms_per_step): one decoder layer of the verify "
@@ -663,6 +697,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--stage-trace", action="store_true", help="print an in-kernel stage breakdown to stderr")
     ap.add_argument("--T", type=int, default=0, help="verify block size (T sweep; default 6)")
+    ap.add_argument("--experts", default="fp8", choices=["fp8", "mxfp4"],
+                    help="routed-expert storage of the stack (the default workload is FP8)")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="KV cache format (the default workload is bf16)")
+    ap.add_argument("--ctx", type=int, default=0, help="cached context of the stream (default 2048)")
     ap.add_argument("--streams", type=int, default=0,
                     help="concurrency workload: S streams of T=6 tokens, contexts U[1024, 8192], seed 4 "
                          "(mk_decode_batch); prints its own line")

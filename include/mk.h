@@ -67,11 +67,18 @@ typedef enum {
 enum {
     MK_DT_F32 = 0,           /* float32                                                 */
     MK_DT_BF16 = 1,          /* bfloat16                                                */
-    MK_DT_FP8E4M3_B128 = 2   /* FP8 E4M3 codes + float32 scale per 1x128 input block:   */
+    MK_DT_FP8E4M3_B128 = 2,  /* FP8 E4M3 codes + float32 scale per 1x128 input block:   */
                              /* W[n][k] = fp8(q[n][k]) * scale[k/128][n]                */
+    MK_DT_FP8E4M3 = 4,       /* FP8 E4M3 codes times one float32 scale per tensor: the  */
+                             /* KV cache (kv_dtype) with a K and a V scale per layer    */
+    MK_DT_MXFP4_B32 = 3      /* MXFP4 (OCP Microscaling Formats v1.0): FP4 E2M1 codes,  */
+                             /* two per byte (element 2j in the low nibble of byte j),  */
+                             /* and one E8M0 scale byte per 1x32 input block:           */
+                             /* W[n][k] = e2m1(q[n][k]) * 2^(scale[k/32][n] - 127).     */
+                             /* Routed experts only (expert_dtype).                     */
 };
 
-#define MK_DESC_VERSION 1
+#define MK_DESC_VERSION 2
 
 /* Model description.  Limits of this build: T <= 8; hidden, expert_inter and
  * n_q_heads*head_dim multiples of 128 and <= 4096; page_size 64;
@@ -79,7 +86,12 @@ enum {
  * top_k <= 8; n_shared 0 or 1.  bf16 / FP8 weights need a bf16 KV cache and
  * head_dim 128.  F32 weights need an F32 router, head_dim 64,
  * (n_q_heads/n_kv_heads)*T <= 16 and hidden, n_q_heads*head_dim,
- * expert_inter <= 2048. */
+ * expert_inter <= 2048.  MXFP4 routed experts need bf16 or FP8 weights
+ * elsewhere and hidden, expert_inter multiples of 256.
+ * Passage for MXFP4 experts: ezolabs "DeepSeek-V4.1-Flash breaks 1,000 tokens
+ * per second for one user", section "Appendix: method", Serving stack
+ * ("MXFP4 expert weights"); al-engr, section "Where the 11.2 ms goes", kernel
+ * table (the fp8 x fp4 expert GEMM). */
 typedef struct {
     int version;              /* MK_DESC_VERSION                                      */
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim;
@@ -91,8 +103,10 @@ typedef struct {
     int max_pages_per_stream; /* page-table row length; bounds positions              */
     int weight_dtype;         /* MK_DT_* of attention and expert matrices             */
     int router_dtype;         /* MK_DT_F32 or MK_DT_BF16                              */
-    int kv_dtype;             /* MK_DT_F32 or MK_DT_BF16                              */
+    int kv_dtype;             /* MK_DT_F32, MK_DT_BF16 or MK_DT_FP8E4M3               */
     int timeout_ms;           /* limit of every device-side wait; 0 means 1000 ms     */
+    int expert_dtype;         /* MK_DT_* of the routed experts (w1, w3, w2): equal to */
+                              /* weight_dtype, or MK_DT_MXFP4_B32                     */
 } mk_model_desc;
 
 /* One layer's weights (dev pointers).  Shapes, with d = head_dim, H = hidden,
@@ -104,7 +118,9 @@ typedef struct {
  *   w1, w3  [E][I][H];  w2 [E][H][I]        routed experts (gate, up, down)
  *   ws1, ws3 [I][H];    ws2 [H][I]          shared expert (NULL when n_shared = 0)
  * FP8 matrices carry a float32 scale array laid out [in/128][out] (for the
- * expert stacks [E][in/128][out]); it is ignored for other dtypes. */
+ * expert stacks [E][in/128][out]); it is ignored for other dtypes.  MXFP4
+ * routed experts store their codes as bytes [E][rows][cols/2] and their E8M0
+ * scales as bytes [E][cols/32][rows] (w1_scale, w3_scale, w2_scale). */
 typedef struct {
     const float *attn_norm;
     const void *w_qkv;  const float *w_qkv_scale;
@@ -112,9 +128,9 @@ typedef struct {
     const float *moe_norm;
     const void *w_router;
     const float *router_bias;
-    const void *w1;     const float *w1_scale;
-    const void *w3;     const float *w3_scale;
-    const void *w2;     const float *w2_scale;
+    const void *w1;     const void *w1_scale;
+    const void *w3;     const void *w3_scale;
+    const void *w2;     const void *w2_scale;
     const void *ws1;    const float *ws1_scale;
     const void *ws3;    const float *ws3_scale;
     const void *ws2;    const float *ws2_scale;
@@ -133,12 +149,19 @@ typedef struct {
  * maps logical page j of a stream (positions j*P .. j*P+P-1) to a physical
  * page.  A step with positions p_t = ctx + t reads positions < ctx and writes
  * K/V of its T tokens at positions ctx..ctx+T-1; the caller then advances ctx
- * by accepted + 1 (rejected slots are overwritten by the next step). */
+ * by accepted + 1 (rejected slots are overwritten by the next step).
+ * An FP8 cache (kv_dtype MK_DT_FP8E4M3) holds E4M3 codes: an entry's value is
+ * code * k_scale[l] (keys) or code * v_scale[l] (values), and the step stores
+ * its new entries as the nearest code (ties to even, saturating at 448) of
+ * value / scale.  Passage: ezolabs, section "Appendix: method", Serving stack
+ * ("an fp8 (e4m3) KV cache"). */
 typedef struct {
     void *const *k_pool;             /* HOST array [n_layers] of dev pointers         */
     void *const *v_pool;
     const int32_t *page_table;       /* dev                                           */
     int n_pages;                     /* physical pages in each pool                   */
+    const float *k_scale;            /* HOST [n_layers] (FP8 cache only; NULL = 1.0)  */
+    const float *v_scale;            /* HOST [n_layers] (FP8 cache only; NULL = 1.0)  */
 } mk_kv_cache;
 
 typedef struct {
@@ -263,7 +286,8 @@ mk_status mk_layer_forward(mk_state *st, int layer, const float *hidden_in, int 
  * device (different streams without ordering, several host threads) race and
  * give wrong results: serialise them.  Each call clears the control block it
  * needs; nothing else must start at zero.  No call allocates device or host
- * memory. */
+ * memory.  It takes no KV scales, so a model with an FP8 KV cache
+ * (kv_dtype MK_DT_FP8E4M3) returns MK_ERR_UNSUPPORTED. */
 mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const mk_layer_weights *lw,
                                    void *k_pool, void *v_pool, const int32_t *page_table,
                                    int n_pages, const float *hidden_in, int T, int ctx,

@@ -24,10 +24,12 @@ struct mk_state {
     CUtensorMap *d_maps = nullptr;      // weight descriptors
     CUtensorMap *d_kvmaps = nullptr;    // [L][2]
     void **d_kpool = nullptr, **d_vpool = nullptr;
+    float *d_kvscale = nullptr;         // [L][2] (K, V) scales of an FP8 cache
     std::vector<void *> allocs;
     Ctrl *ctrl = nullptr;
     // KV binding cache
     std::vector<void *> bound_k, bound_v;
+    std::vector<float> bound_scale;
     int bound_pages = -1;
     // host-buffer entry point staging
     int32_t *d_tok = nullptr, *d_pos = nullptr, *d_acc = nullptr, *d_am = nullptr;
@@ -100,34 +102,78 @@ mk_status encode_map(mk_state *st, CUtensorMap *out, const void *base, int es, l
     return MK_OK;
 }
 
+// E8M0 scales of an MXFP4 matrix or expert stack, bytes [E][groups][rows]
+// (groups = cols/32): boxes of 256 rows x the 8 groups of one 256-column tile
+mk_status encode_scale_map(mk_state *st, CUtensorMap *out, const void *base, long long rows, long long groups,
+                           long long E) {
+    if (!base) return fail(st, MK_ERR_INVALID, "MXFP4 matrix without scales");
+    if (reinterpret_cast<uintptr_t>(base) % 16 || rows % 16)
+        return fail(st, MK_ERR_INVALID, "MXFP4 scales need a 16-byte aligned pointer and rows % 16 == 0");
+    cuuint64_t dims[3] = {(cuuint64_t)rows, (cuuint64_t)groups, (cuuint64_t)E};
+    cuuint64_t strides[2] = {(cuuint64_t)rows, (cuuint64_t)(rows * groups)};
+    cuuint32_t box[3] = {256, 8, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    cuuint32_t rank = E > 1 ? 3 : 2;
+    CUresult r = st->encode(out, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void *>(base), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(st, MK_ERR_CUDA, "cuTensorMapEncodeTiled (scales) failed (%d)", (int)r);
+    return MK_OK;
+}
+
 struct MatSpec {
     const void *w;
-    const float *scale;
+    const void *scale;
     int dtype, rows, cols, E;
 };
 
-mk_status make_mat(mk_state *st, std::vector<CUtensorMap> &maps, std::vector<long long> &map_of,
-                   DMat &d, const MatSpec &s) {
+// A matrix descriptor's fields and its tensor maps: tm[0] for the codes and,
+// for MXFP4, tm[1] for the E8M0 scales (*nmaps says how many).  The map
+// pointers of d are left null; the caller points them at device copies.
+mk_status describe_mat(mk_state *st, DMat &d, const MatSpec &s, CUtensorMap *tm, int *nmaps) {
     memset(&d, 0, sizeof(d));
+    *nmaps = 0;
     if (!s.w) return MK_OK;  // absent (shared expert with n_shared = 0)
+    const bool fp4 = s.dtype == MK_DT_MXFP4_B32;
     d.dtype = s.dtype;
     d.rows = s.rows;
     d.cols = s.cols;
     d.es = dt_size(s.dtype);
+    d.cpk = fp4 ? 256 : 128 / d.es;
     d.n_rg = (s.rows + 255) / 256;
-    d.n_kc = s.cols * d.es / 128;
+    d.n_kc = s.cols / d.cpk;
     d.is3d = s.E > 1;
-    d.scale = s.scale;
+    d.scale = reinterpret_cast<const float *>(s.scale);
     d.scale_estride = (long long)(s.cols / 128) * s.rows;
     if (s.dtype == MK_DT_FP8E4M3_B128) {
         if (!s.scale) return fail(st, MK_ERR_INVALID, "FP8 matrix without scales");
         if (reinterpret_cast<uintptr_t>(s.scale) % 16) return fail(st, MK_ERR_INVALID, "scale pointer not 16-byte aligned");
     }
-    CUtensorMap tm;
-    mk_status r = encode_map(st, &tm, s.w, d.es, s.cols, s.rows, s.E, 256);
+    mk_status r = encode_map(st, &tm[0], s.w, d.es, fp4 ? s.cols / 2 : s.cols, s.rows, s.E, 256);
     if (r != MK_OK) return r;
-    map_of.push_back((long long)maps.size());
-    maps.push_back(tm);
+    *nmaps = 1;
+    if (fp4) {
+        if ((r = encode_scale_map(st, &tm[1], s.scale, s.rows, s.cols / 32, s.E)) != MK_OK) return r;
+        *nmaps = 2;
+    }
+    return MK_OK;
+}
+
+// describe_mat for mk_create: maps are appended to `maps` and d's map pointers
+// hold (index + 1) until the maps have a device copy
+mk_status make_mat(mk_state *st, std::vector<CUtensorMap> &maps, DMat &d, const MatSpec &s) {
+    CUtensorMap tm[2];
+    int n = 0;
+    mk_status r = describe_mat(st, d, s, tm, &n);
+    if (r != MK_OK) return r;
+    if (n >= 1) {
+        d.tmap = reinterpret_cast<const CUtensorMap *>((uintptr_t)(maps.size() + 1));
+        maps.push_back(tm[0]);
+    }
+    if (n == 2) {
+        d.smap = reinterpret_cast<const CUtensorMap *>((uintptr_t)(maps.size() + 1));
+        maps.push_back(tm[1]);
+    }
     return MK_OK;
 }
 
@@ -149,14 +195,15 @@ mk_status check_desc(mk_state *st, const mk_model_desc *d) {
     if (d->n_shared != 0 && d->n_shared != 1) return fail(st, MK_ERR_UNSUPPORTED, "n_shared must be 0 or 1");
     int G = d->n_q_heads / d->n_kv_heads;
     if (G * d->max_T > MK_MAXROWS) return fail(st, MK_ERR_UNSUPPORTED, "(n_q_heads/n_kv_heads)*max_T > 64");
-    if (d->kv_dtype != MK_DT_F32 && d->kv_dtype != MK_DT_BF16) return fail(st, MK_ERR_UNSUPPORTED, "kv_dtype must be F32 or BF16");
+    if (d->kv_dtype != MK_DT_F32 && d->kv_dtype != MK_DT_BF16 && d->kv_dtype != MK_DT_FP8E4M3)
+        return fail(st, MK_ERR_UNSUPPORTED, "kv_dtype must be F32, BF16 or FP8E4M3");
     // all-fp32 models run the FFMA kernel (attention over head_dim 64, f32 or
     // bf16 KV); bf16 / FP8 models run the tensor-core kernel (head_dim 128, bf16 KV)
     if (d->weight_dtype == MK_DT_F32) {
         if (d->head_dim != 64) return fail(st, MK_ERR_UNSUPPORTED, "fp32 weights need head_dim 64");
         if (G * d->max_T > 16) return fail(st, MK_ERR_UNSUPPORTED, "fp32 weights support (n_q_heads/n_kv_heads)*T <= 16");
-    } else if (d->kv_dtype != MK_DT_BF16 || d->head_dim != 128) {
-        return fail(st, MK_ERR_UNSUPPORTED, "bf16 / FP8 weights need a bf16 KV cache and head_dim 128");
+    } else if ((d->kv_dtype != MK_DT_BF16 && d->kv_dtype != MK_DT_FP8E4M3) || d->head_dim != 128) {
+        return fail(st, MK_ERR_UNSUPPORTED, "bf16 / FP8 weights need a bf16 or FP8 KV cache and head_dim 128");
     }
     if (d->weight_dtype < 0 || d->weight_dtype > 2) return fail(st, MK_ERR_UNSUPPORTED, "weight_dtype");
     if ((d->weight_dtype == MK_DT_F32) != (d->router_dtype == MK_DT_F32))
@@ -166,6 +213,13 @@ mk_status check_desc(mk_state *st, const mk_model_desc *d) {
         (d->hidden > 2048 || d->n_q_heads * d->head_dim > 2048 || d->expert_inter > 2048))
         return fail(st, MK_ERR_UNSUPPORTED, "F32 weights need hidden, n_q_heads*head_dim, expert_inter <= 2048");
     if (d->vocab < 0) return fail(st, MK_ERR_INVALID, "vocab < 0");
+    if (d->expert_dtype != d->weight_dtype) {
+        if (d->expert_dtype != MK_DT_MXFP4_B32)
+            return fail(st, MK_ERR_UNSUPPORTED, "expert_dtype must equal weight_dtype or be MXFP4");
+        if (d->weight_dtype == MK_DT_F32) return fail(st, MK_ERR_UNSUPPORTED, "MXFP4 experts need bf16 or FP8 weights elsewhere");
+        if (d->hidden % 256 || d->expert_inter % 256)
+            return fail(st, MK_ERR_UNSUPPORTED, "MXFP4 experts need hidden and expert_inter multiples of 256");
+    }
     return MK_OK;
 }
 
@@ -243,7 +297,6 @@ mk_status mk_create(const mk_model_desc *desc, const mk_weights *w, mk_state **o
     const int E = d.n_experts, I = d.expert_inter, nqkv = (Hq + 2 * Hkv) * hd;
     // descriptors of every weight matrix
     std::vector<CUtensorMap> maps;
-    std::vector<long long> idx;
     std::vector<DLayer> layers(L);
     for (int l = 0; l < L; ++l) {
         const mk_layer_weights &lw = w->layers[l];
@@ -260,9 +313,9 @@ mk_status mk_create(const mk_model_desc *desc, const mk_weights *w, mk_state **o
             {lw.w_qkv, lw.w_qkv_scale, wd, nqkv, H, 1},
             {lw.w_o, lw.w_o_scale, wd, H, Hq * hd, 1},
             {lw.w_router, nullptr, d.router_dtype, E, H, 1},
-            {lw.w1, lw.w1_scale, wd, I, H, E},
-            {lw.w3, lw.w3_scale, wd, I, H, E},
-            {lw.w2, lw.w2_scale, wd, H, I, E},
+            {lw.w1, lw.w1_scale, d.expert_dtype, I, H, E},
+            {lw.w3, lw.w3_scale, d.expert_dtype, I, H, E},
+            {lw.w2, lw.w2_scale, d.expert_dtype, H, I, E},
             {d.n_shared ? lw.ws1 : nullptr, lw.ws1_scale, wd, I, H, 1},
             {d.n_shared ? lw.ws3 : nullptr, lw.ws3_scale, wd, I, H, 1},
             {d.n_shared ? lw.ws2 : nullptr, lw.ws2_scale, wd, H, I, 1},
@@ -270,26 +323,23 @@ mk_status mk_create(const mk_model_desc *desc, const mk_weights *w, mk_state **o
         DMat *dm[9] = {&dl.qkv, &dl.o, &dl.router, &dl.w1, &dl.w3, &dl.w2, &dl.s1, &dl.s3, &dl.s2};
         for (int k = 0; k < 9; ++k) {
             if (k < 6 && !specs[k].w) return bail(fail(st, MK_ERR_INVALID, "layer %d: null weight %d", l, k));
-            // expert stacks of one expert still use the 3-D descriptor shape
-            if (k >= 3 && k <= 5 && E == 1) specs[k].E = 1;
-            r = make_mat(st, maps, idx, *dm[k], specs[k]);
+            r = make_mat(st, maps, *dm[k], specs[k]);
             if (r != MK_OK) return bail(r);
-            if (specs[k].w) dm[k]->tmap = reinterpret_cast<const CUtensorMap *>((uintptr_t)(idx.back() + 1));
         }
     }
     DModel hm;
     memset(&hm, 0, sizeof(hm));
     if (d.vocab > 0) {
         MatSpec s{w->lm_head, nullptr, MK_DT_BF16, d.vocab, H, 1};
-        r = make_mat(st, maps, idx, hm.lm, s);
+        r = make_mat(st, maps, hm.lm, s);
         if (r != MK_OK) return bail(r);
-        hm.lm.tmap = reinterpret_cast<const CUtensorMap *>((uintptr_t)(idx.back() + 1));
     }
     if ((r = dalloc(st, &st->d_maps, maps.size() * sizeof(CUtensorMap))) != MK_OK) return bail(r);
     if (cudaMemcpy(st->d_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice) != cudaSuccess)
         return bail(fail(st, MK_ERR_CUDA, "copy of tensor maps"));
     auto fix = [&](DMat &m) {
         if (m.tmap) m.tmap = st->d_maps + ((uintptr_t)m.tmap - 1);
+        if (m.smap) m.smap = st->d_maps + ((uintptr_t)m.smap - 1);
     };
     for (auto &dl : layers) {
         fix(dl.qkv); fix(dl.o); fix(dl.router); fix(dl.w1); fix(dl.w3); fix(dl.w2);
@@ -348,6 +398,7 @@ mk_status mk_create(const mk_model_desc *desc, const mk_weights *w, mk_state **o
     if ((r = dalloc(st, &st->d_kvmaps, 2 * L * sizeof(CUtensorMap))) != MK_OK) return bail(r);
     if ((r = dalloc(st, &st->d_kpool, L * sizeof(void *))) != MK_OK) return bail(r);
     if ((r = dalloc(st, &st->d_vpool, L * sizeof(void *))) != MK_OK) return bail(r);
+    if ((r = dalloc(st, &st->d_kvscale, 2 * L * sizeof(float))) != MK_OK) return bail(r);
     if ((r = dalloc(st, &st->d_tok, 4 * T8)) != MK_OK) return bail(r);
     if ((r = dalloc(st, &st->d_pos, 4 * T8)) != MK_OK) return bail(r);
     if ((r = dalloc(st, &st->d_acc, 16)) != MK_OK) return bail(r);
@@ -362,9 +413,22 @@ static mk_status bind_kv(mk_state *st, const mk_kv_cache *kv) {
     const int L = d.n_layers;
     if (!kv || !kv->k_pool || !kv->v_pool || !kv->page_table || kv->n_pages < 1)
         return fail(st, MK_ERR_INVALID, "bad kv cache descriptor");
-    bool same = st->bound_pages == kv->n_pages && (int)st->bound_k.size() == L;
+    // (K, V) scales: those of an FP8 cache (absent: 1), 1 for other caches
+    std::vector<float> sc(2 * L, 1.f);
+    if (d.kv_dtype == MK_DT_FP8E4M3) {
+        for (int l = 0; l < L; ++l) {
+            if (kv->k_scale) sc[2 * l] = kv->k_scale[l];
+            if (kv->v_scale) sc[2 * l + 1] = kv->v_scale[l];
+            if (!(sc[2 * l] > 0.f) || !(sc[2 * l + 1] > 0.f) || !std::isfinite(sc[2 * l]) || !std::isfinite(sc[2 * l + 1]))
+                return fail(st, MK_ERR_INVALID, "FP8 KV scales of layer %d must be finite and > 0", l);
+        }
+    }
+    bool same = st->bound_pages == kv->n_pages && (int)st->bound_k.size() == L && st->bound_scale == sc;
     for (int l = 0; same && l < L; ++l) same = st->bound_k[l] == kv->k_pool[l] && st->bound_v[l] == kv->v_pool[l];
     if (same) return MK_OK;
+    // the tables below are read by a step still running on the last stream
+    if (st->launched && cudaStreamSynchronize(st->last_stream) != cudaSuccess)
+        return fail(st, MK_ERR_CUDA, "synchronize before rebinding the KV cache failed");
     const int es = dt_size(d.kv_dtype);
     std::vector<CUtensorMap> maps(2 * L);
     for (int l = 0; l < L; ++l) {
@@ -377,6 +441,8 @@ static mk_status bind_kv(mk_state *st, const mk_kv_cache *kv) {
     CK(cudaMemcpy(st->d_kvmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice));
     CK(cudaMemcpy(st->d_kpool, kv->k_pool, L * sizeof(void *), cudaMemcpyHostToDevice));
     CK(cudaMemcpy(st->d_vpool, kv->v_pool, L * sizeof(void *), cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(st->d_kvscale, sc.data(), 2 * L * sizeof(float), cudaMemcpyHostToDevice));
+    st->bound_scale = sc;
     st->bound_k.assign(kv->k_pool, kv->k_pool + L);
     st->bound_v.assign(kv->v_pool, kv->v_pool + L);
     st->bound_pages = kv->n_pages;
@@ -392,6 +458,7 @@ static mk_status launch(mk_state *st, Params &p, void *stream) {
     p.kvmaps = st->d_kvmaps;
     p.kpool = st->d_kpool;
     p.vpool = st->d_vpool;
+    p.kv_scale = st->d_kvscale;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = mk_launch(p, st->grid, st->smem, s, st->f32);
     if (e != cudaSuccess) return fail(st, MK_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
@@ -638,6 +705,8 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     mk_status r = check_desc(st, desc);
     if (r != MK_OK) return ret(r);
     mk_model_desc d = *desc;
+    if (d.kv_dtype == MK_DT_FP8E4M3)
+        return ret(fail(st, MK_ERR_UNSUPPORTED, "mk_layer_forward_noalloc takes no KV scales: FP8 caches are not supported"));
     if (T < 1 || T > d.max_T) return ret(fail(st, MK_ERR_INVALID, "T = %d outside [1, %d]", T, d.max_T));
     if (ctx < 0 || (long long)ctx + T > (long long)d.max_pages_per_stream * d.page_size)
         return ret(fail(st, MK_ERR_INVALID, "ctx %d + T exceeds the page table", ctx));
@@ -666,7 +735,7 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     Carve cv;
     const size_t o_model = cv.take<DModel>(sizeof(DModel));
     const size_t o_layer = cv.take<DLayer>(sizeof(DLayer));
-    const size_t o_maps = cv.take<CUtensorMap>(11 * sizeof(CUtensorMap));
+    const size_t o_maps = cv.take<CUtensorMap>(14 * sizeof(CUtensorMap));
     const size_t o_pools = cv.take<void *>(2 * sizeof(void *));
     const size_t o_rope = cv.take<float2>(T8 * (hd / 2) * sizeof(float2));
     const size_t o_ctrl = cv.take<Ctrl>(sizeof(Ctrl));
@@ -688,7 +757,9 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     unsigned char *base = nd->scratch;
 
     // descriptors of the layer's matrices and of its KV pools
-    CUtensorMap maps[11];
+    // 9 matrices with up to 3 MXFP4 scale maps, then the K and V pools
+    constexpr int kMatMaps = 12;
+    CUtensorMap maps[kMatMaps + 2];
     DLayer dl;
     memset(&dl, 0, sizeof(dl));
     dl.attn_norm = lw->attn_norm;
@@ -696,11 +767,11 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     dl.router_bias = lw->router_bias;
     if (!lw->attn_norm || !lw->moe_norm || !lw->router_bias) return ret(fail(st, MK_ERR_INVALID, "null norm or bias"));
     if (d.n_shared && (!lw->ws1 || !lw->ws3 || !lw->ws2)) return ret(fail(st, MK_ERR_INVALID, "n_shared = 1 needs ws1/ws3/ws2"));
-    const int wd = d.weight_dtype;
+    const int wd = d.weight_dtype, xd = d.expert_dtype;
     MatSpec specs[9] = {
         {lw->w_qkv, lw->w_qkv_scale, wd, nqkv, H, 1},   {lw->w_o, lw->w_o_scale, wd, H, Hq * hd, 1},
-        {lw->w_router, nullptr, d.router_dtype, E, H, 1}, {lw->w1, lw->w1_scale, wd, I, H, E},
-        {lw->w3, lw->w3_scale, wd, I, H, E},             {lw->w2, lw->w2_scale, wd, H, I, E},
+        {lw->w_router, nullptr, d.router_dtype, E, H, 1}, {lw->w1, lw->w1_scale, xd, I, H, E},
+        {lw->w3, lw->w3_scale, xd, I, H, E},             {lw->w2, lw->w2_scale, xd, H, I, E},
         {d.n_shared ? lw->ws1 : nullptr, lw->ws1_scale, wd, I, H, 1},
         {d.n_shared ? lw->ws3 : nullptr, lw->ws3_scale, wd, I, H, 1},
         {d.n_shared ? lw->ws2 : nullptr, lw->ws2_scale, wd, H, I, 1},
@@ -709,29 +780,16 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     int nmaps = 0;
     for (int k = 0; k < 9; ++k) {
         if (k < 6 && !specs[k].w) return ret(fail(st, MK_ERR_INVALID, "null weight %d", k));
-        DMat &m = *dm[k];
-        memset(&m, 0, sizeof(m));
-        if (!specs[k].w) continue;
-        const MatSpec &sp = specs[k];
-        m.dtype = sp.dtype;
-        m.rows = sp.rows;
-        m.cols = sp.cols;
-        m.es = dt_size(sp.dtype);
-        m.n_rg = (sp.rows + 255) / 256;
-        m.n_kc = sp.cols * m.es / 128;
-        m.is3d = sp.E > 1;
-        m.scale = sp.scale;
-        m.scale_estride = (long long)(sp.cols / 128) * sp.rows;
-        if (sp.dtype == MK_DT_FP8E4M3_B128 && (!sp.scale || reinterpret_cast<uintptr_t>(sp.scale) % 16))
-            return ret(fail(st, MK_ERR_INVALID, "FP8 matrix needs 16-byte aligned scales"));
-        if ((r = encode_map(st, &maps[nmaps], sp.w, m.es, sp.cols, sp.rows, sp.E, 256)) != MK_OK) return ret(r);
-        m.tmap = reinterpret_cast<const CUtensorMap *>(base + o_maps) + nmaps;
-        ++nmaps;
+        int n = 0;
+        if ((r = describe_mat(st, *dm[k], specs[k], &maps[nmaps], &n)) != MK_OK) return ret(r);
+        if (n >= 1) dm[k]->tmap = reinterpret_cast<const CUtensorMap *>(base + o_maps) + nmaps;
+        if (n == 2) dm[k]->smap = reinterpret_cast<const CUtensorMap *>(base + o_maps) + nmaps + 1;
+        nmaps += n;
     }
     const int kv_es = dt_size(d.kv_dtype);
     const long long kv_rows = (long long)n_pages * Hkv * d.page_size;
-    if ((r = encode_map(st, &maps[9], k_pool, kv_es, hd, kv_rows, 1, d.page_size)) != MK_OK) return ret(r);
-    if ((r = encode_map(st, &maps[10], v_pool, kv_es, hd, kv_rows, 1, d.page_size)) != MK_OK) return ret(r);
+    if ((r = encode_map(st, &maps[kMatMaps], k_pool, kv_es, hd, kv_rows, 1, d.page_size)) != MK_OK) return ret(r);
+    if ((r = encode_map(st, &maps[kMatMaps + 1], v_pool, kv_es, hd, kv_rows, 1, d.page_size)) != MK_OK) return ret(r);
 
     // RoPE rows of positions ctx..ctx+T-1 (fp64 angles, stored fp32); the model
     // block points the table so that the kernel's absolute index lands on them
@@ -779,7 +837,7 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     Params p;
     memset(&p, 0, sizeof(p));
     p.m = reinterpret_cast<const DModel *>(base + o_model);
-    p.kvmaps = reinterpret_cast<const CUtensorMap *>(base + o_maps) + 9;
+    p.kvmaps = reinterpret_cast<const CUtensorMap *>(base + o_maps) + kMatMaps;
     p.kpool = reinterpret_cast<void *const *>(base + o_pools);
     p.vpool = reinterpret_cast<void *const *>(base + o_pools) + 1;
     p.page_table = page_table;

@@ -24,10 +24,12 @@
 #define MK_MARKS 1024                    // intra-stage trace events per CTA
 #define MK_FX 4294967296.0f              // fixed-point scale of the cross-CTA accumulators
 
+#define MK_SCALE_SLOT 2048                // block scales of one tile: FP8 256 x fp32, MXFP4 8 x 256 E8M0
+
 // Dynamic shared memory map (bytes).
 #define SM_RING 0
 #define SM_SCALE (SM_RING + MK_RING * MK_SLOT)
-#define SM_SCRATCH (SM_SCALE + MK_RING * 1024)
+#define SM_SCRATCH (SM_SCALE + MK_RING * MK_SCALE_SLOT)
 #define SM_SCRATCH_BYTES 65536
 #define SM_ROUTE (SM_SCRATCH + SM_SCRATCH_BYTES)
 #define SM_ROUTE_BYTES 4096
@@ -43,12 +45,14 @@ enum { ST_QKV = 0, ST_ATT, ST_O, ST_ROUTER, ST_SHA, ST_EXPA, ST_EXPB, ST_LM };
 struct DMat {
     const CUtensorMap *tmap;   // 64-byte aligned descriptor in device memory
     const float *scale;        // FP8: [E][cols/128][rows]
+    const CUtensorMap *smap;   // MXFP4: descriptor of the E8M0 scales [E][cols/32][rows]
     int dtype;                 // MK_DT_*
     int rows, cols;            // per expert
     int n_rg;                  // 256-row groups
     int n_kc;                  // 128-byte column chunks
     int is3d;                  // expert stack
-    int es;                    // element size (bytes)
+    int es;                    // bytes per stored element (MXFP4: a byte holds two)
+    int cpk;                   // columns per 128-byte chunk (MXFP4 256, FP8 128, bf16 64, fp32 32)
     long long scale_estride;   // floats per expert in `scale`
 };
 
@@ -103,6 +107,7 @@ struct Params {
     const CUtensorMap *kvmaps;         // [L][2] (K, V)
     void *const *kpool;                // dev array [L]
     void *const *vpool;
+    const float *kv_scale;             // dev [L][2]: (K, V) scale of an FP8 E4M3 cache
     const int32_t *page_table;
     const int32_t *tokens;
     const int32_t *positions;

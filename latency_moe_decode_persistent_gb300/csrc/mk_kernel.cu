@@ -32,6 +32,7 @@
 // Every wait is bounded by %globaltimer and turns into a status code.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math_constants.h>
 
 #include "mk_internal.h"
@@ -144,6 +145,11 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
                  : "r"(a));
     return v;
 }
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
 __device__ __forceinline__ void ldsm4(uint32_t a, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                       uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -178,6 +184,45 @@ __device__ __forceinline__ void e4m3x4_f16(uint32_t v, uint32_t &lo, uint32_t &h
         " cvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
         : "=r"(lo), "=r"(hi)
         : "r"(v));
+}
+// FP8 E4M3 code of x: nearest, ties to even, saturating at +-448
+__device__ __forceinline__ unsigned char e4m3_code(float x) {
+    return (unsigned char)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+// bytes of a and b picked by selector sel (prmt: a's bytes are 0..3, b's 4..7)
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+// Queries against an FP8 key page: the head dims are taken in a permuted order
+// shared by queries and keys (a dot product does not depend on the order), so
+// that in MMA step kk lane q supplies physical dims 16*(2q + kk/4) + 4*(kk%4) + j
+// from one 4-byte word of a key row.  Logical column (in the f16 query rows the
+// A fragments are loaded from) of physical head dim p:
+__device__ __forceinline__ int q_col_fp8(int p) {
+    const int kk = 4 * ((p >> 4) & 1) + ((p >> 2) & 3), q = p >> 5, j = p & 3;
+    return 16 * kk + 2 * q + (j & 1) + 8 * (j >> 1);
+}
+// two FP4 E2M1 codes (the low 8 bits of v; low nibble first) -> f16x2
+__device__ __forceinline__ uint32_t e2m1x2_f16(uint32_t v) {
+    uint32_t d;
+    asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}\n" : "=r"(d) : "r"(v));
+    return d;
+}
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// 2^d in both halves of an f16x2 word, d <= 0 (subnormal below 2^-14, 0 below 2^-24)
+__device__ __forceinline__ uint32_t pow2_f16x2(int d) {
+    const uint32_t h = d >= -14 ? (uint32_t)(15 + d) << 10 : d >= -24 ? 1u << (24 + d) : 0u;
+    return h | (h << 16);
+}
+// value of an E8M0 scale byte: 2^(e - 127) (0: 2^-127, 255: NaN)
+__device__ __forceinline__ float e8m0_f(int e) {
+    return e == 0 ? __uint_as_float(0x00400000u) : e == 255 ? __uint_as_float(0x7fc00000u) : __uint_as_float((uint32_t)e << 23);
 }
 // two bf16 (low half first) -> f16x2
 __device__ __forceinline__ uint32_t bf16x2_f16x2(uint32_t v) {
@@ -368,7 +413,8 @@ __device__ void raise_err(const Ctx &c, int code, int where) {
     atomicExch(&c.ctrl->abort, 1);
 }
 // a value left the range of the kernel's number formats: an f16 GEMV input
-// beyond 65504 (or NaN), or a partial sum of magnitude 2^31 or more that the
+// beyond 65504 (or NaN), a rotated query beyond it (f16 queries of the FP8 KV
+// attention), or a partial sum of magnitude 2^31 or more that the
 // 2^-32 fixed-point accumulators cannot hold.  The step stops with MK_ERR_RANGE
 // instead of returning infinities or wrapped sums.
 __device__ __noinline__ void range_err(int where) {
@@ -551,6 +597,7 @@ __device__ AttUnit att_unit(const Ctx &c) {
 struct MatR {
     const CUtensorMap *tmap;
     const float *scale;
+    const CUtensorMap *smap;
     long long sest;
     int rows, cols, xstep, dtype, is3d;
 };
@@ -558,6 +605,7 @@ __device__ __forceinline__ MatR mat_regs(const DMat &d) {
     MatR r;
     r.tmap = d.tmap;
     r.scale = d.scale;
+    r.smap = d.smap;
     r.sest = d.scale_estride;
     r.rows = d.rows;
     r.cols = d.cols;
@@ -581,6 +629,7 @@ struct StageIter {
     int n_rg, n_kc, nmat, nex, nd;
     int ex, mat, rg, kc, n;
     int kc0, kcn;         // first column piece of the current chunk; pieces per chunk
+    int kcn_sh;           // down projections: pieces per row group of the shared expert
     int st;
     const int *dlist;
     __device__ __forceinline__ const MatR &cur() const {
@@ -601,6 +650,8 @@ struct StageIter {
                         ex = 0;
                         kc0 += kcn;
                         kc = kc0;
+                    } else if (ex == nd && st == ST_EXPB) {
+                        kcn = kcn_sh;  // the shared expert may be stored in another format
                     }
                 }
             }
@@ -670,11 +721,28 @@ __device__ void stage_iter(StageIter &it, const Ctx &c, int st, const DLayer &L,
                      st == ST_LM ? m.lm : st == ST_SHA ? L.s1 : st == ST_EXPA ? L.w1 : L.w2;
     it.n_rg = d0.n_rg;
     it.n_kc = d0.n_kc;
-    it.kcn = (chunk_major(st) && d0.cols % 1024 == 0) ? 8 * d0.es : it.n_kc;
+    it.kcn = (chunk_major(st) && d0.cols % 1024 == 0) ? 1024 / d0.cpk : it.n_kc;
+    if (st == ST_EXPB) {
+        // items (expert slot, 256-row group), whole items per CTA as below; the
+        // shared expert's items have its own number of column pieces (MXFP4
+        // routed experts: 256 columns a piece, an FP8 shared expert: 128)
+        const int kr = it.kcn, ks = m.nshared ? L.s2.n_kc : kr, nrt = it.nd * it.n_rg;
+        it.kcn_sh = ks;
+        int bi, ei;
+        split_range(it.nex * it.n_rg, c.G, c.cta, bi, ei);
+        it.n = (min(ei, nrt) - min(bi, nrt)) * kr + (max(ei, nrt) - max(bi, nrt)) * ks;
+        it.ex = bi / it.n_rg;
+        it.rg = bi - it.ex * it.n_rg;
+        it.mat = 0;
+        it.kc0 = it.kc = 0;
+        if (it.ex >= it.nd) it.kcn = ks;
+        return;
+    }
+    it.kcn_sh = it.kcn;
     const int nch = it.n_kc / it.kcn;
     const int per_mat = it.n_rg * it.kcn, per_ex = it.nmat * per_mat, per_ch = it.nex * per_ex;
     int b, e;
-    if (st == ST_EXPA || st == ST_EXPB) {
+    if (st == ST_EXPA) {
         // whole items only: an item's partial sum is then formed by one CTA in
         // a fixed tile order whatever the number of routed experts, so the
         // step's result for a token does not depend on the other tokens of
@@ -737,6 +805,7 @@ __device__ __forceinline__ bool prod_gemv_impl(const Ctx &c, Prod &ps, int st, c
         const int e = it.expert();
         uint32_t sbytes = 0;
         if (d.dtype == MK_DT_FP8E4M3_B128) sbytes = min(256, d.rows - it.rg * 256) * 4;
+        else if (d.dtype == MK_DT_MXFP4_B32) sbytes = 8 * 256;  // one box of E8M0 scales
         const uint32_t pos = ps.pi + t, slot = pos % MK_RING;
         if (!prod_take(c, ps, pos, MK_SLOT + sbytes)) {
             ok = false;
@@ -748,9 +817,13 @@ __device__ __forceinline__ bool prod_gemv_impl(const Ctx &c, Prod &ps, int st, c
         if (d.is3d) tma3d_h(dst, d.tmap, x, y, e, &full[slot], ps.pol);
         else tma2d_h(dst, d.tmap, x, y, &full[slot], ps.pol);
         unsigned long long t1 = c.prof ? clock64() : 0;
-        if (sbytes) {
+        if (d.dtype == MK_DT_MXFP4_B32) {
+            // scales [E][cols/32][rows]: the tile's 8 groups x 256 rows
+            if (d.is3d) tma3d_h(sbase + slot * MK_SCALE_SLOT, d.smap, y, it.kc * 8, e, &full[slot], ps.pol);
+            else tma2d_h(sbase + slot * MK_SCALE_SLOT, d.smap, y, it.kc * 8, &full[slot], ps.pol);
+        } else if (sbytes) {
             const float *src = d.scale + (long long)e * d.sest + (long long)it.kc * d.rows + y;
-            bulk_g2s_h(sbase + slot * 1024, src, sbytes, &full[slot], ps.pol);
+            bulk_g2s_h(sbase + slot * MK_SCALE_SLOT, src, sbytes, &full[slot], ps.pol);
         }
         if (c.prof) {
             unsigned long long t2 = clock64();
@@ -886,8 +959,9 @@ __device__ __forceinline__ uint32_t frag_off(int kb, int t, int c4) {
 // build f16 fragments for the 128-column blocks in `mask` (consumer threads).
 // Thread (t, c4) = (tid / 32, tid % 32) converts columns 4*c4 .. 4*c4+3 of
 // token t in every block, so each warp reads one token's block row as whole
-// contiguous L2 lines; eight blocks are in flight before any is converted.
+// contiguous L2 lines.
 // Tokens t >= T get zeros (the MMA reduces against all eight token columns).
+// Four blocks are in flight before any is converted.
 // Blocks in ssq_mask (a subset of mask, residual input only) also get their
 // RMSNorm sum-of-squares partial: warp t sums token t's 128 values of the
 // block (before gamma) and stores it as ssq[which][kb][t].
@@ -900,7 +974,7 @@ __device__ __noinline__ void build_frags(const ActSrc a, uint32_t mask, uint32_t
     const float *f32 = a.f32 ? a.f32 + (long long)t * a.stride + 4 * c4 : nullptr;
     const float *gm = a.gamma ? a.gamma + 4 * c4 : nullptr;
     const uint32_t o_tc = frag_off(0, t, c4);
-    constexpr int B = 8;
+    constexpr int B = 4;  // blocks in flight per thread (8 measured slower: register pressure)
     uint32_t rest = mask, bad = 0;
     while (rest) {
         int kb[B];
@@ -966,10 +1040,12 @@ __device__ __noinline__ void build_act32(const ActSrc a, int K) {
 // k-blocks of a contiguous item range [b, e) over (.., rg, kc) ordered items
 __device__ uint32_t needed_kb(int b, int e, const DMat &d) {
     if (e - b >= d.n_kc) return 0xffffffffu >> (32 - (d.cols / 128));
+    // a chunk of cpk columns covers max(1, cpk / 128) blocks from block kc * cpk / 128
+    const uint32_t span = d.cpk > 128 ? (1u << (d.cpk / 128)) - 1u : 1u;
     uint32_t mask = 0;
     for (int i = b; i < e; ++i) {
         int kc = i % d.n_kc;
-        mask |= 1u << ((kc * (128 / d.es)) / 128);
+        mask |= span << ((kc * d.cpk) / 128);
     }
     return mask;
 }
@@ -1090,7 +1166,7 @@ __device__ __forceinline__ void tile_mma(const Ctx &c, int dtype, int slot, int 
                 mma_f16(k[2 * mt + (s2 & 1)], lo0, lo8, hi0, hi8, fx[s2], fy[s2]);
             }
         }
-        const float *sc = reinterpret_cast<const float *>(c.sm + SM_SCALE + slot * 1024);
+        const float *sc = reinterpret_cast<const float *>(c.sm + SM_SCALE + slot * MK_SCALE_SLOT);
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
             const float s0 = sc[rw + 16 * mt], s8 = sc[rw + 16 * mt + 8];
@@ -1098,6 +1174,64 @@ __device__ __forceinline__ void tile_mma(const Ctx &c, int dtype, int slot, int 
             acc[4 * mt + 1] += (k[2 * mt][1] + k[2 * mt + 1][1]) * s0;
             acc[4 * mt + 2] += (k[2 * mt][2] + k[2 * mt + 1][2]) * s8;
             acc[4 * mt + 3] += (k[2 * mt][3] + k[2 * mt + 1][3]) * s8;
+        }
+    } else if (!kF32 && dtype == MK_DT_MXFP4_B32) {
+        // 256 rows x 256 columns: a 128-byte row holds activation blocks 2kc
+        // and 2kc+1.  Lane q takes 16-byte chunk q of each block, i.e. columns
+        // 32q .. 32q+31, the columns frag_col gives it; in step s it uses the
+        // four codes of word ((s>>1) + 2(q>>1)) & 3, half s & 1.  A 32-column
+        // group has one E8M0 scale, so the four lanes of an MMA step hold four
+        // different scales: each lane multiplies its decoded weights by
+        // 2^(e_q - e_max) in f16 (a power of two, exact unless below 2^-24),
+        // and the block's partial sums take 2^(e_max - 127) afterwards, e_max
+        // being the largest of the row's four group exponents in the block.
+        const unsigned char *sc = c.sm + SM_SCALE + slot * MK_SCALE_SLOT;  // [8 groups][256 rows]
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int kb = 2 * kc + b;
+            const int ch = ((4 * b + q) ^ r) << 4;
+            uint4 a[4];
+            uint32_t fac[4];
+            float sx[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                a[j] = lds128(tile + (rw + 8 * j) * 128 + ch);
+                const int e = sc[(4 * b + q) * 256 + rw + 8 * j];
+                int em = max(e, __shfl_xor_sync(0xffffffffu, e, 1));
+                em = max(em, __shfl_xor_sync(0xffffffffu, em, 2));
+                fac[j] = pow2_f16x2(e - em);
+                sx[j] = e8m0_f(em);
+            }
+            const uint32_t fb = frag + kb * 2048 + c.lane * 16;
+            uint4 f0 = lds128(fb), f1 = lds128(fb + 512), f2 = lds128(fb + 1024), f3 = lds128(fb + 1536);
+            const uint32_t fx[8] = {f0.x, f0.z, f1.x, f1.z, f2.x, f2.z, f3.x, f3.z};
+            const uint32_t fy[8] = {f0.y, f0.w, f1.y, f1.w, f2.y, f2.w, f3.y, f3.w};
+            float k[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) k[i][0] = k[i][1] = k[i][2] = k[i][3] = 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < 8; ++s2) {
+                const int w = ((s2 >> 1) + 2 * (q >> 1)) & 3, sh = 16 * (s2 & 1);
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const uint4 &u0 = a[2 * mt], &u8 = a[2 * mt + 1];
+                    const uint32_t w0 = (w == 0 ? u0.x : w == 1 ? u0.y : w == 2 ? u0.z : u0.w) >> sh;
+                    const uint32_t w8 = (w == 0 ? u8.x : w == 1 ? u8.y : w == 2 ? u8.z : u8.w) >> sh;
+                    const uint32_t lo0 = hmul2u(e2m1x2_f16(w0), fac[2 * mt]);
+                    const uint32_t hi0 = hmul2u(e2m1x2_f16(w0 >> 8), fac[2 * mt]);
+                    const uint32_t lo8 = hmul2u(e2m1x2_f16(w8), fac[2 * mt + 1]);
+                    const uint32_t hi8 = hmul2u(e2m1x2_f16(w8 >> 8), fac[2 * mt + 1]);
+                    mma_f16(k[2 * mt + (s2 & 1)], lo0, lo8, hi0, hi8, fx[s2], fy[s2]);
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const float s0 = sx[2 * mt], s8 = sx[2 * mt + 1];
+                acc[4 * mt + 0] += (k[2 * mt][0] + k[2 * mt + 1][0]) * s0;
+                acc[4 * mt + 1] += (k[2 * mt][1] + k[2 * mt + 1][1]) * s0;
+                acc[4 * mt + 2] += (k[2 * mt][2] + k[2 * mt + 1][2]) * s8;
+                acc[4 * mt + 3] += (k[2 * mt][3] + k[2 * mt + 1][3]) * s8;
+            }
         }
     } else {  // bf16: the tile is half of a 128-column block
         const int h = kc & 1, kb = kc >> 1;
@@ -1500,9 +1634,12 @@ __device__ float qkv_val(const Ctx &c, int t, int col) {
 
 // prepares rotated q (scratch) and, for the unit holding the new block, the
 // block's K/V (scratch + cache append)
-__device__ void att_prepare(const Ctx &c, int l, const AttUnit &u, bool mma_path) {
+template <bool kFP8>
+__device__ __forceinline__ void att_prepare(const Ctx &c, int l, const AttUnit &u, bool mma_path) {
     const DModel &m = *c.m;
     const int G = m.Hq / m.Hkv, R = G * c.T, hd = m.d / 2;
+    constexpr bool fp8kv = kFP8;
+    bool qbad = false;
     unsigned char *scr = c.sm + SM_SCRATCH;
     const long long *qkv = acc_ptr(m, ACC_QKV, c.misc->par);
     // rotated queries: 4 consecutive pairs per item, two items per thread and batch
@@ -1554,7 +1691,14 @@ __device__ void att_prepare(const Ctx &c, int l, const AttUnit &u, bool mma_path
             for (int j = 0; j < 4; ++j) {
                 float a1 = x1[j] * inv, a2 = x2[j] * inv;
                 float y1 = a1 * cs[2 * j] - a2 * cs[2 * j + 1], y2 = a2 * cs[2 * j] + a1 * cs[2 * j + 1];
-                if (mma_path) {
+                if constexpr (fp8kv) {
+                    __half *qs = reinterpret_cast<__half *>(scr);
+                    const __half h1 = __float2half_rn(y1), h2 = __float2half_rn(y2);
+                    qbad |= (__habs(h1) > __float2half_rn(65504.f)) | (__habs(h2) > __float2half_rn(65504.f)) |
+                            __hisnan(h1) | __hisnan(h2);
+                    qs[row * 136 + q_col_fp8(k + j)] = h1;
+                    qs[row * 136 + q_col_fp8(k + j + hd)] = h2;
+                } else if (mma_path) {
                     __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(scr);
                     qs[row * 136 + k + j] = __float2bfloat16_rn(y1);
                     qs[row * 136 + k + j + hd] = __float2bfloat16_rn(y2);
@@ -1566,10 +1710,11 @@ __device__ void att_prepare(const Ctx &c, int l, const AttUnit &u, bool mma_path
             }
         }
     }
-    if (mma_path) {  // zero the padding rows of the last m-tile
-        __nv_bfloat16 *qs = reinterpret_cast<__nv_bfloat16 *>(scr);
+    if (qbad) range_err(331);
+    if (mma_path) {  // zero the padding rows of the last m-tile (zero bits in bf16 and f16)
+        uint16_t *qs = reinterpret_cast<uint16_t *>(scr);
         int R16 = (R + 15) & ~15;
-        for (int i = c.tid; i < (R16 - R) * 136; i += MK_NCWARPS * 32) qs[R * 136 + i] = __float2bfloat16_rn(0.f);
+        for (int i = c.tid; i < (R16 - R) * 136; i += MK_NCWARPS * 32) qs[R * 136 + i] = 0;
     }
     if (!u.has_new) return;
     // block keys / values: mini page after the queries
@@ -1590,7 +1735,24 @@ __device__ void att_prepare(const Ctx &c, int l, const AttUnit &u, bool mma_path
         int pos = c.ctx + t;
         int phys = __ldg(c.p->page_table + pos / m.P);
         long long off = ((long long)(phys * m.Hkv + u.g) * m.P + (pos % m.P)) * m.d;
-        if (kv_es == 2) {
+        if constexpr (kFP8) {
+            // codes of value / scale (nearest, ties to even, saturating at 448)
+            const float ks = c.p->kv_scale[2 * l], vs = c.p->kv_scale[2 * l + 1];
+            const unsigned char kc1 = e4m3_code(k1 / ks), kc2 = e4m3_code(k2 / ks);
+            const unsigned char vc1 = e4m3_code(v1 / vs), vc2 = e4m3_code(v2 / vs);
+            unsigned char *kp = reinterpret_cast<unsigned char *>(c.p->kpool[l]) + off;
+            unsigned char *vp = reinterpret_cast<unsigned char *>(c.p->vpool[l]) + off;
+            kp[k] = kc1;
+            kp[k + hd] = kc2;
+            vp[k] = vc1;
+            vp[k + hd] = vc2;
+            // mini page [16 keys][128 B] swizzled, as the pages of the ring
+            auto put = [&](unsigned char *base, int dd, unsigned char v) { base[swz(0, t, dd)] = v; };
+            put(mini, k, kc1);
+            put(mini, k + hd, kc2);
+            put(mini + 4096, k, vc1);
+            put(mini + 4096, k + hd, vc2);
+        } else if (kv_es == 2) {
             __nv_bfloat16 kb1 = __float2bfloat16_rn(k1), kb2 = __float2bfloat16_rn(k2);
             __nv_bfloat16 vb1 = __float2bfloat16_rn(v1), vb2 = __float2bfloat16_rn(v2);
             __nv_bfloat16 *kp = reinterpret_cast<__nv_bfloat16 *>(c.p->kpool[l]) + off;
@@ -1642,7 +1804,7 @@ struct AttMma {
 // one key page of nkeys (64, or 16 for the block's own keys): kbase/vbase hold
 // [2 boxes][nkeys][128 B] swizzled with box stride bs.  Keys are taken in
 // 32-key halves, each with its own online-softmax update.
-__device__ void att_page_mma(const Ctx &c, AttMma &A, uint32_t kbase, uint32_t vbase, int bs,
+__device__ __forceinline__ void att_page_mma(const Ctx &c, AttMma &A, uint32_t kbase, uint32_t vbase, int bs,
                              int nkeys, int valid, bool causal, int mt, int G) {
     const int r = c.lane >> 2, q = c.lane & 3, mi = c.lane >> 3, li = c.lane & 7;
     const float sl2 = rsqrtf((float)c.m->d) * 1.4426950408889634f;
@@ -1739,6 +1901,124 @@ __device__ void att_page_mma(const Ctx &c, AttMma &A, uint32_t kbase, uint32_t v
     }
 }
 
+// one key page of FP8 E4M3 codes (nkeys 64, or 16 for the block's own keys):
+// kbase / vbase hold [nkeys][128 B] swizzled.  Both products run as f16 MMAs on
+// the codes, which f16 holds exactly; the K scale is part of sl2 (the softmax
+// scale in the log2 domain) and the caller applies the V scale to the output.
+// QK^T: head dims in the order of q_col_fp8, each lane reading two 16-byte
+// chunks of its key row per 32-key half.  PV: output column n of n-tile
+// 4g + np is physical head dim 32g + 4n + np, so a lane builds its B fragments
+// from one 4-byte word (4 dims) of each of its four key rows.
+__device__ __forceinline__ void att_page_fp8(const Ctx &c, AttMma &A, uint32_t kbase, uint32_t vbase, int nkeys, int valid,
+                             bool causal, int mt, int G, float sl2) {
+    const int r = c.lane >> 2, q = c.lane & 3;
+    for (int h0 = 0; h0 < nkeys; h0 += 32) {
+        const int nnt = min(4, (nkeys - h0) >> 3);
+        float sc[4][4];
+        uint4 kw[4][2];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            kw[nt][0] = kw[nt][1] = make_uint4(0, 0, 0, 0);
+            if (nt < nnt) {
+                const int key = h0 + 8 * nt + r;
+                const uint32_t row = kbase + key * 128;
+                kw[nt][0] = lds128(row + (((2 * q) ^ (key & 7)) << 4));
+                kw[nt][1] = lds128(row + (((2 * q + 1) ^ (key & 7)) << 4));
+            }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t q0, q1, q2, q3;
+            ldsm4(A.qaddr + kk * 32, q0, q1, q2, q3);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                if (nt < nnt) {
+                    const uint4 &u = kw[nt][kk >> 2];
+                    const uint32_t w = (kk & 3) == 0 ? u.x : (kk & 3) == 1 ? u.y : (kk & 3) == 2 ? u.z : u.w;
+                    uint32_t lo, hi;
+                    e4m3x4_f16(w, lo, hi);
+                    mma_f16(sc[nt], q0, q1, q2, q3, lo, hi);
+                }
+            }
+        }
+        float mx[2] = {-CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                int key = h0 + 8 * nt + 2 * q + (i & 1);
+                int row = mt * 16 + r + (i >> 1) * 8;
+                bool ok = nt < nnt && key < valid;
+                if (causal) ok = ok && key <= row / G;
+                float v = ok ? sc[nt][i] * sl2 : -CUDART_INF_F;
+                sc[nt][i] = v;
+                mx[i >> 1] = fmaxf(mx[i >> 1], v);
+            }
+        }
+        float corr[2], mn[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+            mn[h] = fmaxf(A.mrow[h], mx[h]);
+            corr[h] = exp2f(A.mrow[h] - mn[h]);
+            A.mrow[h] = mn[h];
+            A.lrow[h] *= corr[h];
+        }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float pv = exp2f(sc[nt][i] - mn[i >> 1]);
+                sc[nt][i] = pv;
+                A.lrow[i >> 1] += pv;
+            }
+        }
+#pragma unroll
+        for (int nd = 0; nd < 16; ++nd) {
+            A.o[nd][0] *= corr[0];
+            A.o[nd][1] *= corr[0];
+            A.o[nd][2] *= corr[1];
+            A.o[nd][3] *= corr[1];
+        }
+#pragma unroll
+        for (int kk2 = 0; kk2 < 2; ++kk2) {
+            if (2 * kk2 < nnt) {
+                const uint32_t a0 = pack_f16(sc[2 * kk2][0], sc[2 * kk2][1]);
+                const uint32_t a1 = pack_f16(sc[2 * kk2][2], sc[2 * kk2][3]);
+                const uint32_t a2 = pack_f16(sc[2 * kk2 + 1][0], sc[2 * kk2 + 1][1]);
+                const uint32_t a3 = pack_f16(sc[2 * kk2 + 1][2], sc[2 * kk2 + 1][3]);
+                // this lane's keys k, k+1 (b0) and k+8, k+9 (b1); keys at or past
+                // `valid` may hold any bits (NaN codes included): read as zero
+                const int k0 = h0 + 16 * kk2 + 2 * q;
+                const int ks[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    uint32_t v[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int key = ks[i];
+                        const uint32_t ad = vbase + key * 128 + (((2 * g + (r >> 2)) ^ (key & 7)) << 4) + 4 * (r & 3);
+                        v[i] = key < valid ? lds32(ad) : 0u;
+                    }
+                    uint32_t b0[4], b1[4];
+                    e4m3x4_f16(prmt(v[0], v[1], 0x5140u), b0[0], b0[1]);
+                    e4m3x4_f16(prmt(v[0], v[1], 0x7362u), b0[2], b0[3]);
+                    e4m3x4_f16(prmt(v[2], v[3], 0x5140u), b1[0], b1[1]);
+                    e4m3x4_f16(prmt(v[2], v[3], 0x7362u), b1[2], b1[3]);
+#pragma unroll
+                    for (int np = 0; np < 4; ++np) mma_f16(A.o[4 * g + np], a0, a1, a2, a3, b0[np], b1[np]);
+                }
+            }
+        }
+    }
+}
+// column (head dim) of output fragment element (n-tile nd, lane quad q, c = 0/1)
+__device__ __forceinline__ int att_ocol(bool fp8kv, int nd, int q, int c) {
+    return fp8kv ? 32 * (nd >> 2) + 8 * q + 4 * c + (nd & 3) : nd * 8 + 2 * q + c;
+}
+
 // FFMA attention of one page for <= 16 rows (fp32 caches, head_dim 64)
 struct AttF {
     float o[16][2];
@@ -1796,6 +2076,8 @@ __device__ void att_page_f32(const Ctx &c, AttF &A, const float *qs, int R, int 
 }
 
 // returns the ring position after this CTA's pages, or -1 if the step aborted
+// (one instance per KV format on the tensor-core path: FP8 pages or bf16 pages)
+template <bool kFP8>
 __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     const Ctx c = make_ctx();
     const DModel &m = *c.m;
@@ -1804,7 +2086,10 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     constexpr bool mma_path = !kF32;
     const int nbox = (m.d * m.kv_es) / 128, bs = m.P * 128;
     const int D2 = m.d + 2;
-    if (u.active) att_prepare(c, l, u, mma_path);
+    constexpr bool fp8kv = mma_path && kFP8;
+    const float ksc = fp8kv ? c.p->kv_scale[2 * l] : 1.f, vsc = fp8kv ? c.p->kv_scale[2 * l + 1] : 1.f;
+    const float sl2 = rsqrtf((float)m.d) * 1.4426950408889634f * ksc;
+    if (u.active) att_prepare<fp8kv>(c, l, u, mma_path);
     bar_consumers();
     mark(c, ST_ATT * 16 + 0);
     unsigned char *scr = c.sm + SM_SCRATCH;
@@ -1828,7 +2113,8 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
             if (ok && wact && ((j - u.p0) % nws) == ws) {
                 int valid = min(m.P, c.ctx - j * m.P);
                 const uint32_t kb = sa(c.sm + SM_RING + ks * MK_SLOT);
-                att_page_mma(c, A, kb, kb + MK_SLOT / 2, bs, 64, valid, false, mt, G);
+                if constexpr (fp8kv) att_page_fp8(c, A, kb, kb + MK_SLOT / 2, 64, valid, false, mt, G, sl2);
+                else att_page_mma(c, A, kb, kb + MK_SLOT / 2, bs, 64, valid, false, mt, G);
             }
             __syncwarp();
             if (c.lane == 0) mbar_arrive(&c.empty[ks]);
@@ -1836,7 +2122,8 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
         }
         if (u.has_new && wact && ((u.pc1 - u.p0) % nws) == ws) {
             uint32_t mini = sa(scr + 17408);
-            att_page_mma(c, A, mini, mini + 4096, 2048, 16, c.T, true, mt, G);
+            if constexpr (fp8kv) att_page_fp8(c, A, mini, mini + 4096, 16, c.T, true, mt, G, sl2);
+            else att_page_mma(c, A, mini, mini + 4096, 2048, 16, c.T, true, mt, G);
         }
         // finish row sums
 #pragma unroll
@@ -1853,10 +2140,11 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
             float *w = mrg + ((ws - 1) * nmt + mt) * WS;
 #pragma unroll
             for (int nd = 0; nd < 16; ++nd) {
-                w[r * 128 + nd * 8 + 2 * q] = A.o[nd][0];
-                w[r * 128 + nd * 8 + 2 * q + 1] = A.o[nd][1];
-                w[(r + 8) * 128 + nd * 8 + 2 * q] = A.o[nd][2];
-                w[(r + 8) * 128 + nd * 8 + 2 * q + 1] = A.o[nd][3];
+                const int c0 = att_ocol(fp8kv, nd, q, 0), c1 = att_ocol(fp8kv, nd, q, 1);
+                w[r * 128 + c0] = A.o[nd][0];
+                w[r * 128 + c1] = A.o[nd][1];
+                w[(r + 8) * 128 + c0] = A.o[nd][2];
+                w[(r + 8) * 128 + c1] = A.o[nd][3];
             }
             if (q == 0) {
                 w[2048 + r] = A.mrow[0];
@@ -1879,8 +2167,8 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
                     A.lrow[h] = A.lrow[h] * a + l2 * b;
 #pragma unroll
                     for (int nd = 0; nd < 16; ++nd) {
-                        A.o[nd][2 * h] = A.o[nd][2 * h] * a + w[rr * 128 + nd * 8 + 2 * q] * b;
-                        A.o[nd][2 * h + 1] = A.o[nd][2 * h + 1] * a + w[rr * 128 + nd * 8 + 2 * q + 1] * b;
+                        A.o[nd][2 * h] = A.o[nd][2 * h] * a + w[rr * 128 + att_ocol(fp8kv, nd, q, 0)] * b;
+                        A.o[nd][2 * h + 1] = A.o[nd][2 * h + 1] * a + w[rr * 128 + att_ocol(fp8kv, nd, q, 1)] * b;
                     }
                 }
             }
@@ -1889,10 +2177,29 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
                 int row = mt * 16 + r + 8 * h;
                 if (row < R) {
                     float *dst = part + row * D2;
+                    if constexpr (fp8kv) {  // the V scale, and 8 consecutive dims 32g + 8q .. +7 per lane
 #pragma unroll
-                    for (int nd = 0; nd < 16; ++nd)
-                        __stcg(reinterpret_cast<float2 *>(dst + nd * 8 + 2 * q),
-                               make_float2(A.o[nd][2 * h], A.o[nd][2 * h + 1]));
+                        for (int g = 0; g < 4; ++g) {
+                            float4 lo, hi;
+                            lo.x = A.o[4 * g][2 * h] * vsc;
+                            lo.y = A.o[4 * g + 1][2 * h] * vsc;
+                            lo.z = A.o[4 * g + 2][2 * h] * vsc;
+                            lo.w = A.o[4 * g + 3][2 * h] * vsc;
+                            hi.x = A.o[4 * g][2 * h + 1] * vsc;
+                            hi.y = A.o[4 * g + 1][2 * h + 1] * vsc;
+                            hi.z = A.o[4 * g + 2][2 * h + 1] * vsc;
+                            hi.w = A.o[4 * g + 3][2 * h + 1] * vsc;
+                            __stcg(reinterpret_cast<float2 *>(dst + 32 * g + 8 * q), make_float2(lo.x, lo.y));
+                            __stcg(reinterpret_cast<float2 *>(dst + 32 * g + 8 * q + 2), make_float2(lo.z, lo.w));
+                            __stcg(reinterpret_cast<float2 *>(dst + 32 * g + 8 * q + 4), make_float2(hi.x, hi.y));
+                            __stcg(reinterpret_cast<float2 *>(dst + 32 * g + 8 * q + 6), make_float2(hi.z, hi.w));
+                        }
+                    } else {
+#pragma unroll
+                        for (int nd = 0; nd < 16; ++nd)
+                            __stcg(reinterpret_cast<float2 *>(dst + nd * 8 + 2 * q),
+                                   make_float2(A.o[nd][2 * h], A.o[nd][2 * h + 1]));
+                    }
                     if (q == 0) {
                         __stcg(dst + m.d, A.mrow[h]);
                         __stcg(dst + m.d + 1, A.lrow[h]);
@@ -2112,7 +2419,7 @@ __device__ __noinline__ void consumer() {
         }
         // ---- attention
         {
-            const long long r = cons_att(l, ci);
+            const long long r = (!kF32 && m.kvdt == MK_DT_FP8E4M3) ? cons_att<true>(l, ci) : cons_att<false>(l, ci);
             if (r < 0) return;
             ci = (uint32_t)r;
         }

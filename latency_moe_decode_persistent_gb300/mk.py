@@ -17,8 +17,8 @@ LIB_PATH = os.path.join(HERE, "libmk.so")
 
 MK_OK, MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_NOMEM = 0, -1, -2, -3
 MK_ERR_TIMEOUT, MK_ERR_CUDA, MK_ERR_BAD_STATE, MK_ERR_BAD_INPUT, MK_ERR_RANGE = -4, -5, -6, -7, -8
-MK_DT_F32, MK_DT_BF16, MK_DT_FP8E4M3_B128 = 0, 1, 2
-MK_DESC_VERSION = 1
+MK_DT_F32, MK_DT_BF16, MK_DT_FP8E4M3_B128, MK_DT_MXFP4_B32, MK_DT_FP8E4M3 = 0, 1, 2, 3, 4
+MK_DESC_VERSION = 2
 
 #: every symbol include/mk.h declares
 EXPORTS = ["mk_create", "mk_decode_step", "mk_decode_batch", "mk_decode_step_host", "mk_layer_forward",
@@ -39,7 +39,7 @@ class mk_model_desc(ctypes.Structure):
                 ("page_size", ctypes.c_int), ("max_T", ctypes.c_int),
                 ("max_pages_per_stream", ctypes.c_int), ("weight_dtype", ctypes.c_int),
                 ("router_dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int),
-                ("timeout_ms", ctypes.c_int)]
+                ("timeout_ms", ctypes.c_int), ("expert_dtype", ctypes.c_int)]
 
 
 class mk_layer_weights(ctypes.Structure):
@@ -56,7 +56,8 @@ class mk_weights(ctypes.Structure):
 
 class mk_kv_cache(ctypes.Structure):
     _fields_ = [("k_pool", ctypes.POINTER(_vp)), ("v_pool", ctypes.POINTER(_vp)),
-                ("page_table", _vp), ("n_pages", ctypes.c_int)]
+                ("page_table", _vp), ("n_pages", ctypes.c_int),
+                ("k_scale", ctypes.POINTER(ctypes.c_float)), ("v_scale", ctypes.POINTER(ctypes.c_float))]
 
 
 class mk_stats(ctypes.Structure):
@@ -245,7 +246,9 @@ class ModelArgs:
             MK_DESC_VERSION, cfg.n_layers, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads,
             cfg.head_dim, cfg.rope_base, cfg.rms_eps, cfg.n_experts, cfg.top_k, cfg.n_shared,
             cfg.expert_inter, cfg.vocab, cfg.page_size, max_T, max_pages, cfg.weight_dtype,
-            cfg.router_dtype, cfg.kv_dtype, timeout_ms)
+            cfg.router_dtype, MK_DT_FP8E4M3 if cfg.kv_dtype == MK_DT_FP8E4M3_B128 else cfg.kv_dtype,
+            timeout_ms,
+            getattr(cfg, "routed_dtype", cfg.weight_dtype))
         n = cfg.n_layers
         self.layers = (mk_layer_weights * n)()
         for i, L in enumerate(model.layers):
@@ -274,10 +277,18 @@ class ModelArgs:
 class KVArgs:
     """mk_kv_cache for pools and a page table held as device tensors."""
 
-    def __init__(self, k_pools: Sequence, v_pools: Sequence, page_table, n_pages: int):
+    def __init__(self, k_pools: Sequence, v_pools: Sequence, page_table, n_pages: int,
+                 scales: Optional[Sequence] = None):
         n = len(k_pools)
         self._k = (_vp * n)(*[_ptr(t) for t in k_pools])
         self._v = (_vp * n)(*[_ptr(t) for t in v_pools])
         self.page_table = page_table
+        ks = vs = None
+        if scales is not None:
+            self._ks = (ctypes.c_float * n)(*[float(a) for a, _ in scales])
+            self._vs = (ctypes.c_float * n)(*[float(b) for _, b in scales])
+            ks = ctypes.cast(self._ks, ctypes.POINTER(ctypes.c_float))
+            vs = ctypes.cast(self._vs, ctypes.POINTER(ctypes.c_float))
         self.kv = mk_kv_cache(ctypes.cast(self._k, ctypes.POINTER(_vp)),
-                              ctypes.cast(self._v, ctypes.POINTER(_vp)), _ptr(page_table), n_pages)
+                              ctypes.cast(self._v, ctypes.POINTER(_vp)), _ptr(page_table), n_pages,
+                              ks, vs)

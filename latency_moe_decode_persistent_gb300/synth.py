@@ -14,6 +14,9 @@ standing in for the real checkpoint and prompts):
   * embedding rows      N(0, 1) (bf16); LM head N(0, 1/H) (bf16)
   * page table          a seeded permutation of physical pages
   * FP8 weights         per 1x128 block: scale = amax/448, code = RNE(w/scale)
+  * MXFP4 expert weights per 1x32 block: E8M0 scale 2^(floor(log2 amax) - 2),
+                        E2M1 code = RNE(w/scale) saturated at +-6, two codes per
+                        byte (element 2j in the low nibble)
 """
 from __future__ import annotations
 
@@ -24,8 +27,8 @@ from typing import List, Optional
 import numpy as np
 import torch
 
-WDT_F32, WDT_BF16, WDT_FP8 = 0, 1, 2
-_KIND = {WDT_F32: "f32", WDT_BF16: "bf16", WDT_FP8: "fp8"}
+WDT_F32, WDT_BF16, WDT_FP8, WDT_MXFP4 = 0, 1, 2, 3
+_KIND = {WDT_F32: "f32", WDT_BF16: "bf16", WDT_FP8: "fp8", WDT_MXFP4: "mxfp4"}
 
 
 @dataclass
@@ -52,10 +55,17 @@ class Config:
     rms_eps: float = 1e-6
     rope_base: float = 10000.0
     gamma_jitter: float = 0.0
+    expert_dtype: int = -1         # routed-expert storage; -1: the same as weight_dtype
+    kv_scales: tuple = (1.0, 1.0)  # FP8 KV cache: (K, V) scale of every layer (value = code * scale),
+                                   # or a list of per-layer (K, V) pairs
 
     @property
     def qkv_rows(self):
         return (self.n_q_heads + 2 * self.n_kv_heads) * self.head_dim
+
+    @property
+    def routed_dtype(self):
+        return self.weight_dtype if self.expert_dtype < 0 else self.expert_dtype
 
 
 def tiny_config(**kw) -> Config:
@@ -141,6 +151,39 @@ def quantize_fp8_blocks(w: torch.Tensor):
     return codes, scale.transpose(-1, -2).contiguous()
 
 
+# E2M1 rounding: the midpoints between the representable magnitudes
+# 0, 0.5, 1, 1.5, 2, 3, 4, 6; a magnitude exactly at a midpoint takes the code
+# with an even mantissa bit (the upper one at 0.75, 1.75 and 3.5)
+_E2M1_MID = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
+_E2M1_TIE_UP = (0.75, 1.75, 3.5)
+
+
+def quantize_mxfp4_blocks(w: torch.Tensor):
+    """Encode w[..., N, K] (fp32) as MXFP4: per 32 consecutive inputs one E8M0
+    scale 2^X with X = floor(log2(amax)) - 2 (so the block's largest magnitude
+    lands in [4, 8) before rounding), elements rounded to E2M1 (nearest, ties
+    to even, saturating at 6).  Returns (packed uint8 [..., N, K/2] with element
+    2j in the low nibble of byte j, scale codes uint8 [..., K/32, N])."""
+    *lead, N, K = w.shape
+    assert K % 32 == 0
+    blocks = w.reshape(*lead, N, K // 32, 32).to(torch.float64)
+    amax = blocks.abs().amax(dim=-1)
+    x = torch.where(amax > 0, torch.floor(torch.log2(amax.clamp_min(1e-300))) - 2, torch.full_like(amax, -127))
+    x = x.clamp(-127, 127)
+    v = blocks / torch.exp2(x).unsqueeze(-1)
+    a = v.abs()
+    code = torch.zeros_like(a, dtype=torch.int64)
+    for m in _E2M1_MID:
+        code += (a > m).to(torch.int64)
+    for m in _E2M1_TIE_UP:
+        code += (a == m).to(torch.int64)
+    code = code.clamp(max=7) + 8 * (v < 0).to(torch.int64)
+    code = code.reshape(*lead, N, K).to(torch.uint8)
+    packed = code[..., 0::2] | (code[..., 1::2] << 4)
+    scale = (x + 127).to(torch.uint8).transpose(-1, -2).contiguous()
+    return packed.contiguous(), scale
+
+
 @dataclass
 class Mat:
     """A stored matrix: ``data`` in the weight dtype (fp32 / bf16 / uint8 FP8 codes),
@@ -174,16 +217,23 @@ def make_matrix(shape, fan_in, wdt, device, seed, *names, chunk=32) -> Mat:
             out[p:e1] = randn((e1 - p,) + tuple(shape[1:]), std, device, seed, *names, p,
                               dtype=torch.bfloat16)
         return Mat(wdt, out)
-    # FP8
+    if wdt == WDT_MXFP4:
+        quant = quantize_mxfp4_blocks
+    else:
+        quant = quantize_fp8_blocks
     if not lead:
-        q, s = quantize_fp8_blocks(randn(shape, std, device, seed, *names))
+        q, s = quant(randn(shape, std, device, seed, *names))
         return Mat(wdt, q, s)
     E, N, K = shape
-    q = torch.empty(shape, dtype=torch.uint8, device=device)
-    s = torch.empty((E, K // 128, N), dtype=torch.float32, device=device)
+    if wdt == WDT_MXFP4:
+        q = torch.empty((E, N, K // 2), dtype=torch.uint8, device=device)
+        s = torch.empty((E, K // 32, N), dtype=torch.uint8, device=device)
+    else:
+        q = torch.empty(shape, dtype=torch.uint8, device=device)
+        s = torch.empty((E, K // 128, N), dtype=torch.float32, device=device)
     for p in parts:
         e1 = min(E, p + chunk)
-        qq, ss = quantize_fp8_blocks(randn((e1 - p, N, K), std, device, seed, *names, p))
+        qq, ss = quant(randn((e1 - p, N, K), std, device, seed, *names, p))
         q[p:e1] = qq
         s[p:e1] = ss
         del qq, ss
@@ -233,9 +283,9 @@ def make_layer(cfg: Config, l: int, device) -> Layer:
         w_router=make_matrix((E, H), H, cfg.router_dtype, device, s, l, "w_router"),
         router_bias=(uniform((E,), -cfg.bias_range, cfg.bias_range, device, s, l, "bias")
                      if cfg.bias_range > 0 else torch.zeros(E, device=device)),
-        w1=make_matrix((E, I, H), H, wd, device, s, l, "w1"),
-        w3=make_matrix((E, I, H), H, wd, device, s, l, "w3"),
-        w2=make_matrix((E, H, I), I, wd, device, s, l, "w2"),
+        w1=make_matrix((E, I, H), H, cfg.routed_dtype, device, s, l, "w1"),
+        w3=make_matrix((E, I, H), H, cfg.routed_dtype, device, s, l, "w3"),
+        w2=make_matrix((E, H, I), I, cfg.routed_dtype, device, s, l, "w2"),
     )
     if cfg.n_shared:
         lay.ws1 = make_matrix((I, H), H, wd, device, s, l, "ws1")
@@ -263,13 +313,15 @@ def make_model(cfg: Config, device) -> Model:
 @dataclass
 class KVCache:
     """Per layer K and V pools [n_pages][Hkv][P][d] plus page tables
-    [n_streams][max_pages]; ``ctx[s]`` cached positions per stream."""
+    [n_streams][max_pages]; ``ctx[s]`` cached positions per stream.  An FP8
+    cache holds uint8 E4M3 codes and ``scales[l]`` = (K scale, V scale)."""
     k_pools: List[torch.Tensor]
     v_pools: List[torch.Tensor]
     page_table: torch.Tensor
     ctx: List[int]
     page_size: int
     max_pages: int
+    scales: Optional[List[tuple]] = None
 
     @property
     def n_pages(self):
@@ -291,9 +343,20 @@ def make_kv(cfg: Config, device, ctxs=None, T=None, extra_pages=0, seed_tag="kv"
     for s_, n in enumerate(need):
         pt[s_, :n] = perm[o:o + n].to(torch.int32)
         o += n
-    kvt = torch.float32 if cfg.kv_dtype == WDT_F32 else torch.bfloat16
     shape = (n_pages, cfg.n_kv_heads, P, cfg.head_dim)
     kp, vp = [], []
+    if cfg.kv_dtype == WDT_FP8:
+        # N(0,1) entries stored as E4M3 codes of value / scale (saturating)
+        per = cfg.kv_scales
+        scales = ([tuple(map(float, per[l])) for l in range(cfg.n_layers)]
+                  if isinstance(per[0], (tuple, list)) else [tuple(map(float, per))] * cfg.n_layers)
+        for l in range(cfg.n_layers):
+            ks, vs = scales[l]
+            for pools, tag, sc in ((kp, "k", ks), (vp, "v", vs)):
+                x = randn(shape, 1.0, device, cfg.seed, seed_tag, l, tag) / sc
+                pools.append(x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8))
+        return KVCache(kp, vp, pt.to(device), ctxs, P, max_pages, scales)
+    kvt = torch.float32 if cfg.kv_dtype == WDT_F32 else torch.bfloat16
     for l in range(cfg.n_layers):
         kp.append(randn(shape, 1.0, device, cfg.seed, seed_tag, l, "k", dtype=kvt))
         vp.append(randn(shape, 1.0, device, cfg.seed, seed_tag, l, "v", dtype=kvt))
@@ -327,6 +390,7 @@ def oracle_kv(kv: KVCache, l: int, stream: int = 0):
     Pools are the stored bits ([n_pages][Hkv][P][d], float32 or uint16 bf16
     bits); the oracle decodes them and follows the page table itself.
     """
-    kind = "f32" if kv.k_pools[l].dtype == torch.float32 else "bf16"
+    dt = kv.k_pools[l].dtype
+    kind = "f32" if dt == torch.float32 else "fp8" if dt == torch.uint8 else "bf16"
     return (kind, _np(kv.k_pools[l]), _np(kv.v_pools[l]),
             kv.page_table[stream].cpu().numpy().astype(np.int64), kv.ctx[stream])

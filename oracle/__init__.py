@@ -43,6 +43,7 @@ import numpy as np
 
 __all__ = [
     "FP8_E4M3_TABLE", "fp8_e4m3_decode", "bf16_decode", "round_to_bf16", "round_to_f32",
+    "E2M1_TABLE", "e2m1_unpack", "e8m0_decode", "round_to_e4m3",
     "Linear", "dequant", "linear", "rmsnorm", "rope", "sigmoid", "silu",
     "attention_gqa", "route", "swiglu", "LayerView", "layer_forward", "stack_forward",
     "accept_count", "tokens_per_second", "step_seconds_from", "argmax_lowest",
@@ -112,6 +113,56 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def round_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round fp64 values to the nearest OCP FP8 E4M3 ("fn") value, ties to even,
+    saturating at +-448 (the format has no infinity), returned as fp64.
+
+    E4M3 keeps 4 significant bits (3 stored); normal numbers reach down to 2^-6
+    and subnormals are multiples of 2^-9.  Pinned (torch's float8 cast, hand
+    ties, saturation)."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros_like(x)
+    nz = (x != 0) & np.isfinite(x)
+    m, e = np.frexp(x[nz])
+    unit_exp = np.maximum(e - 4, -9)
+    out[nz] = np.ldexp(np.round(np.ldexp(x[nz], -unit_exp)), unit_exp)
+    return np.clip(out, -448.0, 448.0)
+
+
+def _e2m1_value(code: int) -> float:
+    """Value of one FP4 E2M1 element (OCP Microscaling Formats v1.0): 1 sign bit,
+    2 exponent bits with bias 1, 1 mantissa bit; exponent field 0 is subnormal
+    (value m/2); there are no infinities or NaN (largest magnitude 6)."""
+    s = (code >> 3) & 1
+    e = (code >> 1) & 3
+    m = code & 1
+    v = m / 2.0 if e == 0 else (1.0 + m / 2.0) * 2.0 ** (e - 1)
+    return -v if s else v
+
+
+#: fp64 value of every FP4 E2M1 code (4 bits), from the format definition above.
+E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def e8m0_decode(codes: np.ndarray) -> np.ndarray:
+    """E8M0 scale bytes -> fp64: 2^(code - 127); 0xFF is NaN (OCP Microscaling
+    Formats v1.0).  Pinned."""
+    c = np.asarray(codes, dtype=np.int64)
+    out = np.ldexp(1.0, c - 127)
+    return np.where(c == 255, np.nan, out)
+
+
+def e2m1_unpack(packed: np.ndarray) -> np.ndarray:
+    """uint8 bytes holding two E2M1 codes each -> fp64 element values along the
+    last axis, doubled in length.  Reading of the storage layout: element 2j
+    is the low nibble of byte j and element 2j+1 its high nibble.  Pinned."""
+    b = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.float64)
+    out[..., 0::2] = E2M1_TABLE[b & 0xF]
+    out[..., 1::2] = E2M1_TABLE[b >> 4]
+    return out
+
+
 def round_to_f32(x: np.ndarray) -> np.ndarray:
     """Round fp64 to the nearest binary32 value (ties to even), returned as fp64.
 
@@ -134,6 +185,10 @@ class Linear:
                  [in/128][out]; the real weight is
                  W[n][k] = fp8(q[n][k]) * scale[k // 128][n]
                  (1 x 128 blocks along the input dimension).
+    kind "mxfp4": q is uint8 [out][in/2], two FP4 E2M1 codes per byte (element
+                 2j in the low nibble of byte j); scale is uint8 E8M0 [in/32][out];
+                 W[n][k] = e2m1(code[n][k]) * 2^(scale[k // 32][n] - 127)
+                 (MXFP4: 1 x 32 blocks along the input dimension).
     """
     kind: str
     q: np.ndarray
@@ -155,6 +210,11 @@ def dequant(lin: Linear, rows: Optional[slice] = None) -> np.ndarray:
         s = lin.scale if rows is None else lin.scale[:, rows]
         w = fp8_e4m3_decode(q)                        # [n][in]
         blk = np.repeat(s.T.astype(np.float64), 128, axis=1)   # [n][in]
+        return w * blk[:, : w.shape[1]]
+    if lin.kind == "mxfp4":
+        s = lin.scale if rows is None else lin.scale[:, rows]
+        w = e2m1_unpack(q)                            # [n][in]
+        blk = np.repeat(e8m0_decode(s.T), 32, axis=1)   # [n][in]
         return w * blk[:, : w.shape[1]]
     raise ValueError(f"unknown weight kind {lin.kind}")
 
@@ -336,12 +396,12 @@ class Dims:
     expert_inter: int
     rms_eps: float = 1e-6
     rope_base: float = 10000.0
-    kv_dtype: str = "bf16"          # "bf16" | "f32"
+    kv_dtype: str = "bf16"          # "bf16" | "f32" | "fp8" (e4m3 codes times a per-layer scale)
 
 
 def layer_forward(x: np.ndarray, lw: LayerView, dims: Dims, k_ctx: np.ndarray,
                   v_ctx: np.ndarray, ctx: int,
-                  route_hook: Optional[Callable] = None):
+                  route_hook: Optional[Callable] = None, kv_scale=(1.0, 1.0)):
     """One pre-norm decoder layer for a verify block of T tokens.
 
     x [T][H] residual input; k_ctx, v_ctx [Hkv][ctx][d] cached entries.
@@ -367,8 +427,13 @@ def layer_forward(x: np.ndarray, lw: LayerView, dims: Dims, k_ctx: np.ndarray,
     v = qkv[:, (Hq + Hkv) * d:].reshape(T, Hkv, d)
     q = rope(q, pos[:, None], dims.rope_base)
     k = rope(k, pos[:, None], dims.rope_base)
-    rnd = round_to_bf16 if dims.kv_dtype == "bf16" else round_to_f32
-    k_new, v_new = rnd(k), rnd(v)
+    if dims.kv_dtype == "fp8":
+        # stored as e4m3 codes of value / scale, read back as code * scale
+        k_new = round_to_e4m3(k / kv_scale[0]) * kv_scale[0]
+        v_new = round_to_e4m3(v / kv_scale[1]) * kv_scale[1]
+    else:
+        rnd = round_to_bf16 if dims.kv_dtype == "bf16" else round_to_f32
+        k_new, v_new = rnd(k), rnd(v)
     o = attention_gqa(q, k_ctx, v_ctx, k_new, v_new)            # [T][Hq][d]
     h = x + linear(lw.w_o, o.reshape(T, Hq * d))
     z = rmsnorm(h, lw.moe_norm, dims.rms_eps)
@@ -394,7 +459,7 @@ def layer_forward(x: np.ndarray, lw: LayerView, dims: Dims, k_ctx: np.ndarray,
     if lw.shared is not None:
         moe += swiglu(lw.shared[0], lw.shared[1], lw.shared[2], z)
     x_out = h + moe
-    info = dict(k_new=k_new, v_new=v_new, idx=idx, w=w, key=key, s=s, attn=o, h=h,
+    info = dict(k_new=k_new, v_new=v_new, k_rot=k, v_raw=v, idx=idx, w=w, key=key, s=s, attn=o, h=h,
                 z=z, logits_router=logits, overridden=overridden,
                 distinct=len(set(int(v_) for v_ in idx.ravel())))
     return x_out, info
@@ -434,7 +499,7 @@ def step_seconds_from(tokens_per_step: float, tok_per_s: float) -> float:
 def stack_forward(tokens: Sequence[int], embed: np.ndarray, layers: Sequence[LayerView],
                   final_norm: np.ndarray, lm_head: Linear, dims: Dims,
                   kv_ctx: Sequence, ctx: int, route_hook_factory=None,
-                  on_layer: Optional[Callable] = None):
+                  on_layer: Optional[Callable] = None, kv_scales: Optional[Sequence] = None):
     """Full verify step: embedding, L layers, final norm, LM head, argmax, accept.
 
     tokens [T] int (d_0..d_k); embed: callable(token ids) -> fp64 rows [T][H]
@@ -449,7 +514,8 @@ def stack_forward(tokens: Sequence[int], embed: np.ndarray, layers: Sequence[Lay
     infos = []
     for l, lw in enumerate(layers):
         hook = route_hook_factory(l) if route_hook_factory is not None else None
-        x, info = layer_forward(x, lw, dims, kv_ctx[l][0], kv_ctx[l][1], ctx, hook)
+        x, info = layer_forward(x, lw, dims, kv_ctx[l][0], kv_ctx[l][1], ctx, hook,
+                                kv_scale=kv_scales[l] if kv_scales is not None else (1.0, 1.0))
         infos.append(info)
         if on_layer is not None:
             on_layer(l, x, info)
@@ -461,20 +527,24 @@ def stack_forward(tokens: Sequence[int], embed: np.ndarray, layers: Sequence[Lay
 
 
 def kv_from_pool(kind: str, k_pool: np.ndarray, v_pool: np.ndarray,
-                 page_table: np.ndarray, ctx: int):
+                 page_table: np.ndarray, ctx: int, scales=(1.0, 1.0)):
     """Decode a stream's cached K/V (stored bits) and follow its page table.
 
-    kind "bf16": pools hold uint16 bfloat16 bits; "f32": float32 values.
+    kind "bf16": pools hold uint16 bfloat16 bits; "f32": float32 values; "fp8":
+    uint8 E4M3 codes, read as code * scale (scales = (K scale, V scale)).
     Returns (k_ctx, v_ctx), each fp64 [Hkv][ctx][d].  Pinned (a hand-built pool
     whose entries name their page, head and slot, read through a permuted
     page table).
     """
-    dec = bf16_decode if kind == "bf16" else (lambda a: np.asarray(a, dtype=np.float64))
+    if kind == "fp8":
+        dec = fp8_e4m3_decode
+    else:
+        dec = bf16_decode if kind == "bf16" else (lambda a: np.asarray(a, dtype=np.float64))
     P = k_pool.shape[2]
     n_log = (ctx + P - 1) // P
     pt = np.asarray(page_table[:n_log], dtype=np.int64)
-    return (gather_paged(dec(k_pool[pt]), np.arange(n_log), ctx),
-            gather_paged(dec(v_pool[pt]), np.arange(n_log), ctx))
+    return (gather_paged(dec(k_pool[pt]), np.arange(n_log), ctx) * scales[0],
+            gather_paged(dec(v_pool[pt]), np.arange(n_log), ctx) * scales[1])
 
 
 def linear_from(kind: str, q: np.ndarray, scale=None) -> Linear:

@@ -27,7 +27,7 @@ class Built:
         self.args = mk.ModelArgs(self.model, self.max_T, self.kv.max_pages, timeout_ms)
         self.st = mk.mk_create(self.args.desc, self.args.weights)
         self.kvargs = mk.KVArgs(self.kv.k_pools, self.kv.v_pools, self.kv.page_table,
-                                self.kv.n_pages)
+                                self.kv.n_pages, self.kv.scales)
 
     def close(self):
         mk.mk_destroy(self.st)
@@ -108,7 +108,8 @@ def oracle_layer(b: Built, x, l=0, gpu_idx=None, log=None):
     lv = helpers.layer_view(b.model, l)
     kc, vc = helpers.kv_view(b.kv, l)
     hook = tie_hook(gpu_idx, cfg.top_k, log if log is not None else []) if gpu_idx is not None else None
-    return oracle.layer_forward(np.asarray(x, dtype=np.float64), lv, dims, kc, vc, b.kv.ctx[0], hook)
+    return oracle.layer_forward(np.asarray(x, dtype=np.float64), lv, dims, kc, vc, b.kv.ctx[0], hook,
+                                kv_scale=helpers.kv_scales(b.kv)[l])
 
 
 def check_routing(info, gpu_idx, K, where=""):

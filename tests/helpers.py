@@ -6,9 +6,9 @@ from latency_moe_decode_persistent_gb300 import synth
 
 
 def oracle_dims(cfg: synth.Config) -> oracle.Dims:
+    kvk = {synth.WDT_F32: "f32", synth.WDT_BF16: "bf16", synth.WDT_FP8: "fp8"}[cfg.kv_dtype]
     return oracle.Dims(cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.n_experts,
-                       cfg.top_k, cfg.expert_inter, cfg.rms_eps, cfg.rope_base,
-                       "f32" if cfg.kv_dtype == synth.WDT_F32 else "bf16")
+                       cfg.top_k, cfg.expert_inter, cfg.rms_eps, cfg.rope_base, kvk)
 
 
 def lin(m, e=None):
@@ -40,7 +40,12 @@ def layer_view(model: synth.Model, l: int, expert_cache=None) -> oracle.LayerVie
 
 def kv_view(kv: synth.KVCache, l: int, stream: int = 0):
     kind, kp, vp, pt, ctx = synth.oracle_kv(kv, l, stream)
-    return oracle.kv_from_pool(kind, kp, vp, pt, ctx)
+    return oracle.kv_from_pool(kind, kp, vp, pt, ctx, kv.scales[l] if kv.scales else (1.0, 1.0))
+
+
+def kv_scales(kv: synth.KVCache):
+    """Per-layer (K, V) scales for the oracle's stack or layer calls."""
+    return kv.scales if kv.scales else [(1.0, 1.0)] * len(kv.k_pools)
 
 
 def embed_fn(model):

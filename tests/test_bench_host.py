@@ -68,3 +68,30 @@ def test_planned_tokens_per_step_follow_the_draws():
     assert bench.draft_plan(32, 5, 129280, seed=3) == plan
     big = bench.draft_plan(bench.DRAFT_BLOCKS, 5, 129280, seed=3)
     assert abs(bench.tokens_per_step_of(big) - 3.96) < 0.15
+
+
+def test_algorithmic_bytes_with_mxfp4_experts():
+    # MXFP4 routed experts: half a byte per weight plus one E8M0 byte per 32
+    # inputs and output row; attention, router and shared expert stay FP8
+    from latency_moe_decode_persistent_gb300 import synth
+    fp8 = synth.stack_config(T=6, ctx=2048)
+    fp4 = synth.stack_config(T=6, ctx=2048, expert_dtype=synth.WDT_MXFP4)
+    routed_fp8 = 2 * (512 * 4096 + 32 * 512 * 4) + (4096 * 512 + 4 * 4096 * 4)
+    routed_fp4 = 2 * (512 * 4096 // 2 + 128 * 512) + (4096 * 512 // 2 + 16 * 4096)
+    assert routed_fp4 == 3342336
+    d = 1874
+    assert bench.algorithmic_bytes(fp8, d, 2048) - bench.algorithmic_bytes(fp4, d, 2048) == d * (routed_fp8 - routed_fp4)
+
+
+def test_fp8_kv_workload_bytes_and_name():
+    # an FP8 KV cache moves one byte per cached element instead of two: 43 layers
+    # x ctx x 4 kv heads x 128 dims x (K, V), plus the block's own entries
+    from latency_moe_decode_persistent_gb300 import synth
+    b16 = synth.stack_config(T=6, ctx=65536)
+    f8 = synth.stack_config(T=6, ctx=65536, kv_dtype=synth.WDT_FP8, kv_scales=bench.FP8_KV_SCALES)
+    d = 1874
+    diff = bench.algorithmic_bytes(b16, d, 65536) - bench.algorithmic_bytes(f8, d, 65536)
+    assert diff == 43 * (65536 + 6) * 4 * 128 * 2
+    w = bench.workload_of(f8)
+    assert "ctx 65536" in w and "FP8 e4m3 KV (per-layer K/V scales 0.0125/0.0125)" in w
+    assert bench.workload_of(synth.stack_config()) == bench.WORKLOAD

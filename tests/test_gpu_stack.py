@@ -44,7 +44,8 @@ def compare_step(b: gc.Built, toks):
     r = oracle.stack_forward(toks, helpers.embed_fn(b.model), layers,
                              b.model.final_norm.cpu().numpy().astype(np.float64),
                              helpers.lm_head_lin(b.model), dims, kvs, b.kv.ctx[0],
-                             route_hook_factory=lambda l: gc.tie_hook(tr[l], cfg.top_k, log))
+                             route_hook_factory=lambda l: gc.tie_hook(tr[l], cfg.top_k, log),
+                             kv_scales=helpers.kv_scales(b.kv))
     wt = b.wtrace.cpu().numpy()
     for l, info in enumerate(r["layers"]):
         gc.check_routing(info, tr[l], cfg.top_k, where="layer %d" % l)
@@ -82,6 +83,31 @@ def test_mini_stack_edges(T, ctx):
     b = gc.Built(cfg)
     try:
         toks = [int(v) for v in np.random.default_rng(T).integers(0, cfg.vocab, T)]
+        err, acc, r, log = compare_step(b, toks)
+        assert err < gc.TOL[synth.WDT_FP8], err
+    finally:
+        b.close()
+
+
+def test_mini_stack_mxfp4_experts():
+    cfg = mini_stack(expert_dtype=synth.WDT_MXFP4, seed=24, hidden=1024, expert_inter=256)
+    b = gc.Built(cfg)
+    try:
+        toks = make_drafts(b, 33, cfg.T - 1, 0.83, seed=6)
+        err, acc, r, log = compare_step(b, toks)
+        assert err < gc.TOL[synth.WDT_FP8], err
+    finally:
+        b.close()
+
+
+def test_mini_stack_fp8_kv_cache():
+    """FP8 E4M3 KV cache with a different (K, V) scale in every layer, through the
+    whole verify step."""
+    cfg = mini_stack(kv_dtype=synth.WDT_FP8, seed=25, ctx=700,
+                     kv_scales=[(0.0125, 0.02), (0.03, 0.01), (0.02, 0.0125)])
+    b = gc.Built(cfg)
+    try:
+        toks = make_drafts(b, 35, cfg.T - 1, 0.83, seed=7)
         err, acc, r, log = compare_step(b, toks)
         assert err < gc.TOL[synth.WDT_FP8], err
     finally:

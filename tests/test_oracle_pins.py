@@ -71,6 +71,70 @@ def test_f32_round_ties_to_even():
     assert oracle.round_to_f32(np.array([0.1875]))[0] == 0.1875
 
 
+def test_mxfp4_points_from_spec():
+    g = json.load(open(os.path.join(GOLD, "mxfp4_points.json")))
+    assert g["block"] == 32
+    for code, val in g["e2m1"]:
+        got = oracle.E2M1_TABLE[int(code, 16)]
+        assert got == val and math.copysign(1, got) == math.copysign(1, val), code
+    for code, val in g["e8m0"]:
+        assert oracle.e8m0_decode(np.array([int(code, 16)]))[0] == val, code
+    for code in g["e8m0_nan"]:
+        assert np.isnan(oracle.e8m0_decode(np.array([int(code, 16)]))[0])
+
+
+def test_e8m0_matches_torch():
+    codes = torch.arange(255, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e8m0fnu).float().double().numpy()
+    assert np.array_equal(oracle.e8m0_decode(np.arange(255)), ref)
+
+
+def test_e2m1_nibble_order():
+    # byte 0x21: element 0 is the low nibble (0x1 = 0.5), element 1 the high
+    # nibble (0x2 = 1.0); byte 0xF7: 6.0 then -6.0
+    got = oracle.e2m1_unpack(np.array([[0x21, 0xF7]], dtype=np.uint8))
+    assert got.tolist() == [[0.5, 1.0, 6.0, -6.0]]
+
+
+def test_mxfp4_linear_exact_on_small_values():
+    # every E2M1 value times 2 is an integer and E8M0 scales are powers of two,
+    # so a 1 x 32 block-scaled product is exact in fp64 and must equal an
+    # integer computation scaled per block
+    N, K = 12, 96
+    codes = rng.integers(0, 16, size=(N, K))
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    sc = rng.integers(120, 131, size=(K // 32, N)).astype(np.uint8)
+    x = rng.integers(-4, 5, size=(3, K)).astype(np.float64)
+    got = oracle.linear(oracle.Linear("mxfp4", packed, sc), x)
+    twice = np.array([int(round(2 * oracle.E2M1_TABLE[c])) for c in range(16)], dtype=np.int64)
+    w2 = twice[codes]                                     # 2 * element value, integer
+    want = np.zeros((3, N))
+    for kb in range(K // 32):
+        part = x[:, kb * 32:(kb + 1) * 32].astype(np.int64) @ w2[:, kb * 32:(kb + 1) * 32].T
+        want += part * np.ldexp(1.0, sc[kb].astype(np.int64) - 127 - 1)[None, :]
+    assert np.array_equal(got, want)
+
+
+def test_e4m3_rounding_matches_torch_and_ties():
+    x = rng.standard_normal(20000) * np.exp(rng.uniform(-12, 6, 20000))
+    x = x[np.abs(x) <= 448.0].astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).float().double().numpy()
+    assert np.array_equal(oracle.round_to_e4m3(x), ref)
+    # 1 + 2^-4 lies halfway between 1 and 1.125: the even significand (1) wins;
+    # 1 + 3 * 2^-4 lies halfway between 1.125 and 1.25: 1.25 wins
+    assert oracle.round_to_e4m3(np.array([1 + 2 ** -4, 1 + 3 * 2 ** -4])).tolist() == [1.0, 1.25]
+    # subnormal grid 2^-9; 2^-10 is halfway between 0 and 2^-9 -> 0
+    assert oracle.round_to_e4m3(np.array([2.0 ** -10, 3 * 2.0 ** -10])).tolist() == [0.0, 2 * 2.0 ** -9]
+    # no infinity: beyond 448 the result saturates
+    assert oracle.round_to_e4m3(np.array([1000.0, -1e9])).tolist() == [448.0, -448.0]
+
+
+def test_kv_from_pool_fp8_scales():
+    codes = np.array([[[[0x38, 0x40]]]], dtype=np.uint8)   # e4m3 1.0 and 2.0
+    k, v = oracle.kv_from_pool("fp8", codes, codes, np.array([0]), 1, scales=(0.5, 4.0))
+    assert k[0, 0].tolist() == [0.5, 1.0] and v[0, 0].tolist() == [4.0, 8.0]
+
+
 # ---------------------------------------------------------------- linear/dequant
 def test_fp8_linear_exact_on_integer_weights():
     # codes for the integers 1..8 and their negatives, power-of-two block scales:
