@@ -49,6 +49,8 @@ def workload_of(cfg):
         w = w.replace("bf16 KV", "FP8 e4m3 KV (per-layer K/V scales %g/%g)" % tuple(cfg.kv_scales))
     if cfg.ctx != 2048:
         w = w.replace("ctx 2048", "ctx %d" % cfg.ctx)
+    if cfg.lm_dtype == 2:
+        w = w.replace("(bf16 embed/LM head)", "(bf16 embed, FP8 e4m3 1x128 LM head)")
     if cfg.n_layers == 43 and cfg.T == 6:
         return w
     return w.replace("43-layer", "%d-layer" % cfg.n_layers).replace(
@@ -65,6 +67,8 @@ def variant_kw(args, synth):
         kw["kv_scales"] = FP8_KV_SCALES
     if args.ctx:
         kw["ctx"] = args.ctx
+    if args.lm == "fp8":
+        kw["lm_dtype"] = synth.WDT_FP8
     return kw
 
 
@@ -176,7 +180,8 @@ def algorithmic_bytes(cfg, distinct_per_step, ctx):
                  + (shared if cfg.n_shared else 0)
                  + ctx * cfg.n_kv_heads * d * 2 * kv_es + cfg.T * cfg.n_kv_heads * d * 2 * kv_es)
     total = cfg.n_layers * per_layer + distinct_per_step * expert
-    total += cfg.T * H * 2 + H * 4 + cfg.vocab * H * 2 + cfg.T * cfg.vocab * 4
+    lm = fp8(cfg.vocab, H) if cfg.lm_dtype == 2 else cfg.vocab * H * 2
+    total += cfg.T * H * 2 + H * 4 + lm + cfg.T * cfg.vocab * 4
     return total
 
 
@@ -431,7 +436,8 @@ def run_mk(args):
                    if args.experts == "fp8" else
                    "mxfp4 routed experts, fp8e4m3 attention/shared weights x f16 activations -> fp32 "
                    "(bf16 LM head), int64 fixed-point reductions")
-                  + ("; fp8e4m3 KV codes x f16 queries / probabilities" if args.kv == "fp8" else "")),
+                  + ("; fp8e4m3 KV codes x f16 queries / probabilities" if args.kv == "fp8" else "")
+                  + ("; fp8e4m3 1x128 LM head" if args.lm == "fp8" else "")),
         "data": "synthetic (seeded random weights of the named architecture)",
         "config": {"workload": workload_of(cfg), "global_batch": world, "seq_len": T,
                    "parallelism": "replicas (1 stream per GPU)" if world > 1 else "single GPU",
@@ -702,6 +708,8 @@ def main():
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="KV cache format (the default workload is bf16)")
     ap.add_argument("--ctx", type=int, default=0, help="cached context of the stream (default 2048)")
+    ap.add_argument("--lm", default="bf16", choices=["bf16", "fp8"],
+                    help="LM head storage (the default workload is bf16)")
     ap.add_argument("--streams", type=int, default=0,
                     help="concurrency workload: S streams of T=6 tokens, contexts U[1024, 8192], seed 4 "
                          "(mk_decode_batch); prints its own line")

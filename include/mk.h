@@ -78,7 +78,7 @@ enum {
                              /* Routed experts only (expert_dtype).                     */
 };
 
-#define MK_DESC_VERSION 2
+#define MK_DESC_VERSION 3
 
 /* Model description.  Limits of this build: T <= 8; hidden, expert_inter and
  * n_q_heads*head_dim multiples of 128 and <= 4096; page_size 64;
@@ -107,6 +107,8 @@ typedef struct {
     int timeout_ms;           /* limit of every device-side wait; 0 means 1000 ms     */
     int expert_dtype;         /* MK_DT_* of the routed experts (w1, w3, w2): equal to */
                               /* weight_dtype, or MK_DT_MXFP4_B32                     */
+    int lm_head_dtype;        /* MK_DT_BF16, or MK_DT_FP8E4M3_B128 with bf16 / FP8    */
+                              /* weights elsewhere                                    */
 } mk_model_desc;
 
 /* One layer's weights (dev pointers).  Shapes, with d = head_dim, H = hidden,
@@ -136,11 +138,16 @@ typedef struct {
     const void *ws2;    const float *ws2_scale;
 } mk_layer_weights;
 
+/* The LM head is bf16 or, with lm_head_dtype MK_DT_FP8E4M3_B128, FP8 E4M3
+ * codes [vocab][H] with float32 scales lm_head_scale [H/128][vocab].  Passage:
+ * al-engr, section "Where the 11.2 ms goes" (the lm_head's bf16 weight reads)
+ * and section "Credits" (an FP8 draft head). */
 typedef struct {
     const void *embed;               /* bf16 [vocab][H] (dev; NULL if vocab == 0)     */
     const float *final_norm;         /* float32 [H]                                   */
-    const void *lm_head;             /* bf16 [vocab][H]                               */
+    const void *lm_head;             /* [vocab][H] in lm_head_dtype                   */
     const mk_layer_weights *layers;  /* HOST array of n_layers entries                */
+    const float *lm_head_scale;      /* FP8 LM head only: float32 [H/128][vocab]      */
 } mk_weights;
 
 /* Paged KV cache.  Layer l keeps k_pool[l], v_pool[l] (dev), each
@@ -211,6 +218,29 @@ mk_status mk_decode_step(mk_state *st, const int32_t *draft_tokens, int T,
                          const int32_t *positions, const mk_kv_cache *kv,
                          float *out_logits, int32_t *out_accepted, int32_t *out_argmax,
                          void *stream);
+
+/* mk_decode_step with verification by sampling at temperature t (top-p 1)
+ * instead of by argmax.  The drafts are taken as greedy proposals (a point
+ * mass on each draft), for which speculative sampling accepts draft d_i with
+ * probability p_{i-1}(d_i), p_i = softmax(logits_i / t):
+ *   uniforms      dev float32 [T], each in [0, 1): draft i is accepted while
+ *                 every earlier one was and uniforms[i-1] < p_{i-1}(d_i)
+ *                 (i = 1..T-1); uniforms[T-1] draws the emitted token
+ *   out_accepted  dev int32 [1]: n, the accepted drafts
+ *   out_token     dev int32 [1]: the token emitted after d_1..d_n, drawn by
+ *                 inverse CDF in token-id order from p_n without d_{n+1} (renormalised)
+ *                 after a rejection, or from p_{T-1} when every draft was accepted
+ *   out_logits    as mk_decode_step (before the temperature)
+ * The probabilities are formed in float32 (maxima and sums of exp over the
+ * vocabulary slices, combined in a fixed order).  temperature must lie in
+ * [1e-3, 1e3] (else MK_ERR_INVALID).  The emitted tokens are distributed as
+ * sampling the model one token at a time.
+ * Passage: ezolabs, section "Appendix: method", Decode speed (temperature 1.0,
+ * top-p 1.0); section "How we got here" (block verification). */
+mk_status mk_decode_step_sample(mk_state *st, const int32_t *draft_tokens, int T,
+                                const int32_t *positions, const mk_kv_cache *kv, float temperature,
+                                const float *uniforms, float *out_logits, int32_t *out_accepted,
+                                int32_t *out_token, void *stream);
 
 /* One verify step for each of n_streams independent streams (the concurrency
  * workload): stream s has its own block of T tokens, positions ctx_s .. ctx_s+T-1

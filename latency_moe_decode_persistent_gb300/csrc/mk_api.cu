@@ -213,6 +213,10 @@ mk_status check_desc(mk_state *st, const mk_model_desc *d) {
         (d->hidden > 2048 || d->n_q_heads * d->head_dim > 2048 || d->expert_inter > 2048))
         return fail(st, MK_ERR_UNSUPPORTED, "F32 weights need hidden, n_q_heads*head_dim, expert_inter <= 2048");
     if (d->vocab < 0) return fail(st, MK_ERR_INVALID, "vocab < 0");
+    if (d->lm_head_dtype != MK_DT_BF16 && d->lm_head_dtype != MK_DT_FP8E4M3_B128)
+        return fail(st, MK_ERR_UNSUPPORTED, "lm_head_dtype must be BF16 or FP8E4M3_B128");
+    if (d->lm_head_dtype == MK_DT_FP8E4M3_B128 && d->weight_dtype == MK_DT_F32)
+        return fail(st, MK_ERR_UNSUPPORTED, "an FP8 LM head needs bf16 or FP8 weights elsewhere");
     if (d->expert_dtype != d->weight_dtype) {
         if (d->expert_dtype != MK_DT_MXFP4_B32)
             return fail(st, MK_ERR_UNSUPPORTED, "expert_dtype must equal weight_dtype or be MXFP4");
@@ -330,7 +334,7 @@ mk_status mk_create(const mk_model_desc *desc, const mk_weights *w, mk_state **o
     DModel hm;
     memset(&hm, 0, sizeof(hm));
     if (d.vocab > 0) {
-        MatSpec s{w->lm_head, nullptr, MK_DT_BF16, d.vocab, H, 1};
+        MatSpec s{w->lm_head, w->lm_head_scale, d.lm_head_dtype, d.vocab, H, 1};
         r = make_mat(st, maps, hm.lm, s);
         if (r != MK_OK) return bail(r);
     }
@@ -391,6 +395,8 @@ mk_status mk_create(const mk_model_desc *desc, const mk_weights *w, mk_state **o
     if ((r = dalloc(st, &hm.att_part, 4ull * Hkv * MK_MAXSPLIT * MK_MAXROWS * (hd + 2))) != MK_OK) return bail(r);
     if ((r = dalloc(st, &hm.cand_v, 4 * T8 * st->grid)) != MK_OK) return bail(r);
     if ((r = dalloc(st, &hm.cand_i, 4 * T8 * st->grid)) != MK_OK) return bail(r);
+    if ((r = dalloc(st, &hm.cand_m, 4 * T8 * st->grid)) != MK_OK) return bail(r);
+    if ((r = dalloc(st, &hm.cand_s, 4 * T8 * st->grid)) != MK_OK) return bail(r);
     if (cudaMemset(st->ctrl, 0, sizeof(Ctrl)) != cudaSuccess) return bail(fail(st, MK_ERR_CUDA, "memset ctrl"));
     if ((r = dalloc(st, &st->d_model, sizeof(DModel))) != MK_OK) return bail(r);
     if (cudaMemcpy(st->d_model, &hm, sizeof(DModel), cudaMemcpyHostToDevice) != cudaSuccess)
@@ -488,6 +494,36 @@ mk_status mk_decode_step(mk_state *st, const int32_t *draft_tokens, int T, const
     p.out_logits = out_logits;
     p.out_accepted = out_accepted;
     p.out_argmax = out_argmax;
+    p.trace = st->trace;
+    p.wtrace = st->wtrace;
+    return launch(st, p, stream);
+}
+
+mk_status mk_decode_step_sample(mk_state *st, const int32_t *draft_tokens, int T, const int32_t *positions,
+                                const mk_kv_cache *kv, float temperature, const float *uniforms,
+                                float *out_logits, int32_t *out_accepted, int32_t *out_token, void *stream) {
+    if (!st) return MK_ERR_INVALID;
+    if (st->desc.vocab <= 0) return fail(st, MK_ERR_BAD_STATE, "model has no LM head (vocab = 0)");
+    if (T < 1 || T > st->desc.max_T) return fail(st, MK_ERR_INVALID, "T = %d outside [1, %d]", T, st->desc.max_T);
+    if (!draft_tokens || !positions || !out_logits || !out_accepted || !uniforms || !out_token)
+        return fail(st, MK_ERR_INVALID, "null pointer argument");
+    if (!(temperature >= 1e-3f && temperature <= 1e3f))
+        return fail(st, MK_ERR_INVALID, "temperature must lie in [1e-3, 1e3]");
+    mk_status r = bind_kv(st, kv);
+    if (r != MK_OK) return r;
+    Params p;
+    memset(&p, 0, sizeof(p));
+    p.page_table = kv->page_table;
+    p.tokens = draft_tokens;
+    p.positions = positions;
+    p.T = T;
+    p.mode = 0;
+    p.n_pages = kv->n_pages;
+    p.out_logits = out_logits;
+    p.out_accepted = out_accepted;
+    p.temperature = temperature;
+    p.uniforms = uniforms;
+    p.out_token = out_token;
     p.trace = st->trace;
     p.wtrace = st->wtrace;
     return launch(st, p, stream);
@@ -751,6 +787,8 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     const size_t o_part = cv.take<float>(4ull * Hkv * MK_MAXSPLIT * MK_MAXROWS * (hd + 2));
     const size_t o_candv = cv.take<float>(4 * T8 * nd->grid);
     const size_t o_candi = cv.take<int>(4 * T8 * nd->grid);
+    const size_t o_candm = cv.take<float>(4 * T8 * nd->grid);
+    const size_t o_cands = cv.take<float>(4 * T8 * nd->grid);
     if (cv.off > MK_NOALLOC_SCRATCH_BYTES)
         return ret(fail(st, MK_ERR_UNSUPPORTED, "model needs %zu bytes of scratch; mk_layer_forward_noalloc has %u",
                         cv.off, (unsigned)MK_NOALLOC_SCRATCH_BYTES));
@@ -822,6 +860,8 @@ extern "C" mk_status mk_layer_forward_noalloc(const mk_model_desc *desc, const m
     hm.att_part = reinterpret_cast<float *>(base + o_part);
     hm.cand_v = reinterpret_cast<float *>(base + o_candv);
     hm.cand_i = reinterpret_cast<int *>(base + o_candi);
+    hm.cand_m = reinterpret_cast<float *>(base + o_candm);
+    hm.cand_s = reinterpret_cast<float *>(base + o_cands);
     void *pools[2] = {k_pool, v_pool};
 
     // stage the launch's tables into the array (stream-ordered copies; the host

@@ -100,6 +100,7 @@ struct DModel {
     float *att_part;                   // [Hkv][MAXSPLIT][MAXROWS][d+2] attention split partials
     float *cand_v;                     // [G][MAXT] argmax candidates
     int *cand_i;
+    float *cand_m, *cand_s;            // [G][MAXT] sampling: slice maximum and sum of exp (log2 domain)
 };
 
 struct Params {
@@ -118,6 +119,9 @@ struct Params {
     float *out_logits;
     int32_t *out_accepted;
     int32_t *out_argmax;
+    float temperature;                 // > 0: verification by sampling (mk_decode_step_sample)
+    const float *uniforms;             // sampling: [T] accept tests, then the draw
+    int32_t *out_token;                // sampling: the drawn token
     const float *hidden_in;
     float *hidden_out;
     int32_t *out_idx;

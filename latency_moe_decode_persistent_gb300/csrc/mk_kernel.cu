@@ -204,11 +204,14 @@ __device__ __forceinline__ int q_col_fp8(int p) {
     const int kk = 4 * ((p >> 4) & 1) + ((p >> 2) & 3), q = p >> 5, j = p & 3;
     return 16 * kk + 2 * q + (j & 1) + 8 * (j >> 1);
 }
-// two FP4 E2M1 codes (the low 8 bits of v; low nibble first) -> f16x2
-__device__ __forceinline__ uint32_t e2m1x2_f16(uint32_t v) {
-    uint32_t d;
-    asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}\n" : "=r"(d) : "r"(v));
-    return d;
+// eight FP4 E2M1 codes (byte i of v holds codes 2i, 2i+1, low nibble first)
+// -> four f16x2 words, d_i from byte i
+__device__ __forceinline__ void e2m1x8_f16(uint32_t v, uint32_t &d0, uint32_t &d1, uint32_t &d2, uint32_t &d3) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+        : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+        : "r"(v));
 }
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
     uint32_t d;
@@ -567,7 +570,7 @@ __device__ int stage_total(const DModel &m, int st, const DLayer &L, const Route
         case ST_ROUTER: return L.router.n_rg * L.router.n_kc;
         case ST_SHA: return m.nshared ? 2 * L.s1.n_rg * L.s1.n_kc : 0;
         case ST_EXPA: return rt->nd * 2 * L.w1.n_rg * L.w1.n_kc;
-        case ST_EXPB: return (rt->nd + m.nshared) * L.w2.n_rg * L.w2.n_kc;
+        case ST_EXPB: return rt->nd * L.w2.n_rg * L.w2.n_kc + (m.nshared ? L.s2.n_rg * L.s2.n_kc : 0);
         case ST_LM: return m.lm.n_rg * m.lm.n_kc;
     }
     return 0;
@@ -791,6 +794,7 @@ __device__ __forceinline__ bool prod_take(const Ctx &c, Prod &ps, uint32_t pos, 
 }
 
 
+
 __device__ __forceinline__ bool prod_gemv_impl(const Ctx &c, Prod &ps, int st, const DLayer &L,
                                                const RouteSm *rt) {
     StageIter it;
@@ -989,9 +993,13 @@ __device__ __noinline__ void build_frags(const ActSrc a, uint32_t mask, uint32_t
             g[u] = make_float4(1.f, 1.f, 1.f, 1.f);
             if (kb[u] >= 0 && live) {
                 const int col = kb[u] * 128;
-                if (fx) {
-                    x0[u] = __ldcg(reinterpret_cast<const longlong2 *>(fx + col));
-                    x1[u] = __ldcg(reinterpret_cast<const longlong2 *>(fx + col) + 1);
+                if (fx) {  // one 256-bit load (the 32 bytes are 32-byte aligned)
+                    long long v0, v1, v2, v3;
+                    asm volatile("ld.global.cg.v4.b64 {%0,%1,%2,%3}, [%4];"
+                                 : "=l"(v0), "=l"(v1), "=l"(v2), "=l"(v3)
+                                 : "l"(fx + col));
+                    x0[u] = make_longlong2(v0, v1);
+                    x1[u] = make_longlong2(v2, v3);
                 } else {
                     xf[u] = __ldcg(reinterpret_cast<const float4 *>(f32 + col));
                 }
@@ -1196,6 +1204,9 @@ __device__ __forceinline__ void tile_mma(const Ctx &c, int dtype, int slot, int 
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 a[j] = lds128(tile + (rw + 8 * j) * 128 + ch);
+                // word w of the chunk serves steps 2w' and 2w'+1 with w = (w' + 2(q>>1)) & 3:
+                // rotate once so that word w' sits at index w'
+                if (q & 2) a[j] = make_uint4(a[j].z, a[j].w, a[j].x, a[j].y);
                 const int e = sc[(4 * b + q) * 256 + rw + 8 * j];
                 int em = max(e, __shfl_xor_sync(0xffffffffu, e, 1));
                 em = max(em, __shfl_xor_sync(0xffffffffu, em, 2));
@@ -1210,18 +1221,23 @@ __device__ __forceinline__ void tile_mma(const Ctx &c, int dtype, int slot, int 
 #pragma unroll
             for (int i = 0; i < 4; ++i) k[i][0] = k[i][1] = k[i][2] = k[i][3] = 0.f;
 #pragma unroll
-            for (int s2 = 0; s2 < 8; ++s2) {
-                const int w = ((s2 >> 1) + 2 * (q >> 1)) & 3, sh = 16 * (s2 & 1);
+            for (int w = 0; w < 4; ++w) {
 #pragma unroll
                 for (int mt = 0; mt < 2; ++mt) {
                     const uint4 &u0 = a[2 * mt], &u8 = a[2 * mt + 1];
-                    const uint32_t w0 = (w == 0 ? u0.x : w == 1 ? u0.y : w == 2 ? u0.z : u0.w) >> sh;
-                    const uint32_t w8 = (w == 0 ? u8.x : w == 1 ? u8.y : w == 2 ? u8.z : u8.w) >> sh;
-                    const uint32_t lo0 = hmul2u(e2m1x2_f16(w0), fac[2 * mt]);
-                    const uint32_t hi0 = hmul2u(e2m1x2_f16(w0 >> 8), fac[2 * mt]);
-                    const uint32_t lo8 = hmul2u(e2m1x2_f16(w8), fac[2 * mt + 1]);
-                    const uint32_t hi8 = hmul2u(e2m1x2_f16(w8 >> 8), fac[2 * mt + 1]);
-                    mma_f16(k[2 * mt + (s2 & 1)], lo0, lo8, hi0, hi8, fx[s2], fy[s2]);
+                    const uint32_t w0 = w == 0 ? u0.x : w == 1 ? u0.y : w == 2 ? u0.z : u0.w;
+                    const uint32_t w8 = w == 0 ? u8.x : w == 1 ? u8.y : w == 2 ? u8.z : u8.w;
+                    uint32_t p0[4], p8[4];
+                    e2m1x8_f16(w0, p0[0], p0[1], p0[2], p0[3]);
+                    e2m1x8_f16(w8, p8[0], p8[1], p8[2], p8[3]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        p0[i] = hmul2u(p0[i], fac[2 * mt]);
+                        p8[i] = hmul2u(p8[i], fac[2 * mt + 1]);
+                    }
+                    // steps 2w (bytes 0, 1) and 2w + 1 (bytes 2, 3)
+                    mma_f16(k[2 * mt], p0[0], p8[0], p0[1], p8[1], fx[2 * w], fy[2 * w]);
+                    mma_f16(k[2 * mt + 1], p0[2], p8[2], p0[3], p8[3], fx[2 * w + 1], fy[2 * w + 1]);
                 }
             }
 #pragma unroll
@@ -1419,6 +1435,7 @@ __device__ __noinline__ uint32_t cons_gemv(int st, const DLayer *Lp, const Route
     mark(c, st * 16 + 2);
     return ci;
 }
+
 
 // ------------------------------------------------------------------ small helpers
 __device__ __noinline__ void zero_slice_nc(long long *p, long long n) {
@@ -2360,6 +2377,140 @@ __device__ __forceinline__ void copy_layer(const Ctx &c, DLayer *dst, const DLay
     copy_layer_nc(dst, src);
 }
 
+// fold (m2, s2) into (m, s): s = s 2^(m - M) + s2 2^(m2 - M), M = max(m, m2);
+// an empty side has m = -inf and s = 0
+__device__ __forceinline__ void lse_fold(float &m, float &s, float m2, float s2) {
+    const float M = fmaxf(m, m2);
+    if (M == -CUDART_INF_F) return;
+    s = (m == -CUDART_INF_F ? 0.f : s * exp2f(m - M)) + (m2 == -CUDART_INF_F ? 0.f : s2 * exp2f(m2 - M));
+    m = M;
+}
+
+// Verification by sampling, after the per-CTA slice maxima and sums are in
+// place (out of line, and like every out-of-line routine here it rebuilds the
+// thread's context itself instead of taking the caller's by reference).  Every CTA combines the slices in the same fixed order, so all reach
+// the same probabilities, accept count n and draw target; the CTA whose
+// vocabulary slice holds the target scans it and writes the drawn token.
+// Returns n (the caller's CTA 0 reports it).
+__device__ __noinline__ int sample_verify_step() {
+    const Ctx c = make_ctx();
+    const DModel &m = *c.m;
+    const Params &p = *c.p;
+    const float kt = 1.4426950408889634f / p.temperature;
+    float *rowm = reinterpret_cast<float *>(c.sm + SM_SCRATCH + 16384);  // [T] max (log2 domain)
+    float *rowz = rowm + MK_MAXT;                                          // [T] sum of 2^(y - max)
+    int *sh = reinterpret_cast<int *>(rowz + MK_MAXT);                     // n, owner, excluded token
+    float *shf = reinterpret_cast<float *>(sh + 4);                        // slice base, target
+    float *part = shf + 4;                                                 // [threads] scan partials
+    if (c.warp < c.T) {  // warp t: row t over the CTAs' slices, lanes strided, then a fixed tree
+        const int t = c.warp;
+        float mx = -CUDART_INF_F, sm = 0.f;
+        for (int k = c.lane; k < c.G; k += 32)
+            lse_fold(mx, sm, __ldcg(m.cand_m + k * MK_MAXT + t), __ldcg(m.cand_s + k * MK_MAXT + t));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) lse_fold(mx, sm, __shfl_xor_sync(0xffffffffu, mx, o),
+                                              __shfl_xor_sync(0xffffffffu, sm, o));
+        if (c.lane == 0) {
+            rowm[t] = mx;
+            rowz[t] = sm;
+        }
+    }
+    bar_consumers();
+    if (c.tid == 0) {
+        int n = 0;
+        for (int i = 1; i < c.T; ++i) {
+            const int d = __ldg(p.tokens + i);
+            const float pd = exp2f(__ldcg(p.out_logits + (long long)(i - 1) * m.V + d) * kt - rowm[i - 1]) / rowz[i - 1];
+            if (__ldg(p.uniforms + i - 1) < pd) n = i;
+            else break;
+        }
+        const int r = n, ex = n < c.T - 1 ? __ldg(p.tokens + n + 1) : -1;
+        const float Mr = rowm[r];
+        const float wex = ex >= 0 ? exp2f(__ldcg(p.out_logits + (long long)r * m.V + ex) * kt - Mr) : 0.f;
+        const float target = __ldg(p.uniforms + c.T - 1) * (rowz[r] - wex);
+        // the slice holding the target, by the slices' sums in CTA order
+        float acc = 0.f, base = 0.f;
+        int owner = -1, last = 0;
+        for (int k = 0; k < c.G; ++k) {
+            int b, e;
+            split_range(m.V, c.G, k, b, e);
+            const float mk = __ldcg(m.cand_m + k * MK_MAXT + r);
+            float sk = mk == -CUDART_INF_F ? 0.f : __ldcg(m.cand_s + k * MK_MAXT + r) * exp2f(mk - Mr);
+            if (ex >= b && ex < e) sk = fmaxf(sk - wex, 0.f);
+            if (sk > 0.f) last = k;
+            if (owner < 0 && acc + sk > target) {
+                owner = k;
+                base = acc;
+            }
+            acc += sk;
+        }
+        if (owner < 0) {  // the target at the very top (rounding): the last slice with weight
+            owner = last;
+            int b, e;
+            split_range(m.V, c.G, last, b, e);
+            const float mk = __ldcg(m.cand_m + last * MK_MAXT + r);
+            float sk = __ldcg(m.cand_s + last * MK_MAXT + r) * exp2f(mk - Mr);
+            if (ex >= b && ex < e) sk = fmaxf(sk - wex, 0.f);
+            base = acc - sk;
+        }
+        sh[0] = n;
+        sh[1] = owner;
+        sh[2] = ex;
+        shf[0] = base;
+        shf[1] = target;
+    }
+    bar_consumers();
+    const int n = sh[0];
+    if (c.cta != sh[1]) return n;
+    // the owner: contiguous runs of its slice per thread, partial sums in index
+    // order, then the first run whose cumulative sum passes the target
+    const int r = n, ex = sh[2];
+    const float Mr = rowm[r], base = shf[0], target = shf[1];
+    int b, e;
+    split_range(m.V, c.G, c.cta, b, e);
+    const int nth = MK_NCWARPS * 32, len = e - b, run = (len + nth - 1) / nth;
+    const int x0 = b + c.tid * run, x1 = min(e, x0 + run);
+    const float *lg = p.out_logits + (long long)r * m.V;
+    float ps = 0.f;
+    for (int x = x0; x < x1; ++x)
+        if (x != ex) ps += exp2f(__ldcg(lg + x) * kt - Mr);
+    part[c.tid] = ps;
+    bar_consumers();
+    if (c.tid == 0) {
+        float cum = base;
+        int tok = -1, lastx = -1;
+        for (int j = 0; j < nth && tok < 0; ++j) {
+            const int y0 = b + j * run, y1 = min(e, y0 + run);
+            if (y0 >= y1) break;
+            if (cum + part[j] > target) {
+                for (int x = y0; x < y1; ++x) {
+                    if (x == ex) continue;
+                    const float w = exp2f(__ldcg(lg + x) * kt - Mr);
+                    if (w > 0.f) lastx = x;
+                    cum += w;
+                    if (cum > target) {
+                        tok = x;
+                        break;
+                    }
+                }
+                if (tok < 0) tok = lastx;  // rounding between the run's sum and its terms
+            } else {
+                cum += part[j];
+                if (part[j] > 0.f) {
+                    for (int x = y1 - 1; x >= y0; --x)
+                        if (x != ex) {
+                            lastx = x;
+                            break;
+                        }
+                }
+            }
+        }
+        if (tok < 0) tok = lastx >= 0 ? lastx : b;
+        *p.out_token = tok;
+    }
+    return n;
+}
+
 __device__ __noinline__ void consumer() {
     const Ctx c = make_ctx();
     const DModel &m = *c.m;
@@ -2373,8 +2524,9 @@ __device__ __noinline__ void consumer() {
     // layer's copy while it waits at the barrier that ends its QKV stage
     zero_accs(0);
     if (p.mode == 0) zero_slice(c, m.logit_acc, (long long)c.T * m.V);
-    if (c.cta == 0)
+    if (c.cta == 0) {
         for (int i = c.tid; i < m.L * m.Hkv; i += MK_NCWARPS * 32) __stcg(m.att_cnt + i, 0);
+    }
     {
         long long n = (long long)c.T * m.H;
         long long b = n * c.cta / c.G, e = n * (c.cta + 1) / c.G;
@@ -2511,10 +2663,16 @@ __device__ __noinline__ void consumer() {
         split_range(m.V, c.G, c.cta, b, e);
         float best[MK_MAXT];
         int besti[MK_MAXT];
+        // sampling: running maximum and sum of 2^(y - max) of y = logit * log2(e) / t
+        const bool samp = p.temperature > 0.f;
+        const float kt = samp ? 1.4426950408889634f / p.temperature : 0.f;
+        float smx[MK_MAXT], ssum[MK_MAXT];
 #pragma unroll
         for (int t = 0; t < MK_MAXT; ++t) {
             best[t] = -CUDART_INF_F;
             besti[t] = 0x7fffffff;
+            smx[t] = -CUDART_INF_F;
+            ssum[t] = 0.f;
         }
         for (int v0 = b + c.tid; v0 < e; v0 += 4 * MK_NCWARPS * 32) {
             long long raw[4][MK_MAXT];
@@ -2538,6 +2696,15 @@ __device__ __noinline__ void consumer() {
                         best[t] = lg;
                         besti[t] = v;
                     }
+                    if (samp) {
+                        const float y = lg * kt;
+                        if (y > smx[t]) {
+                            ssum[t] = ssum[t] * exp2f(smx[t] - y) + 1.f;
+                            smx[t] = y;
+                        } else {
+                            ssum[t] += exp2f(y - smx[t]);
+                        }
+                    }
                 }
             }
         }
@@ -2559,6 +2726,20 @@ __device__ __noinline__ void consumer() {
                 bi[t * 8 + c.warp] = bi2;
             }
         }
+        float *sv = reinterpret_cast<float *>(c.sm + SM_SCRATCH + 12288);  // [T][8] max, [T][8] sum
+        if (samp) {
+#pragma unroll
+            for (int t = 0; t < MK_MAXT; ++t) {
+                float mx = smx[t], sm = ssum[t];
+#pragma unroll
+                for (int o = 16; o; o >>= 1) lse_fold(mx, sm, __shfl_xor_sync(0xffffffffu, mx, o),
+                                                      __shfl_xor_sync(0xffffffffu, sm, o));
+                if (c.lane == 0 && t < c.T) {
+                    sv[t * 8 + c.warp] = mx;
+                    sv[64 + t * 8 + c.warp] = sm;
+                }
+            }
+        }
         bar_consumers();
         if (c.tid < c.T) {
             int t = c.tid;
@@ -2574,9 +2755,17 @@ __device__ __noinline__ void consumer() {
             }
             __stcg(m.cand_v + c.cta * MK_MAXT + t, best);
             __stcg(m.cand_i + c.cta * MK_MAXT + t, besti);
+            if (samp) {
+                float mx = -CUDART_INF_F, sm = 0.f;
+                for (int w = 0; w < MK_NCWARPS; ++w) lse_fold(mx, sm, sv[t * 8 + w], sv[64 + t * 8 + w]);
+                __stcg(m.cand_m + c.cta * MK_MAXT + t, mx);
+                __stcg(m.cand_s + c.cta * MK_MAXT + t, sm);
+            }
         }
     }
     if (!grid_sync(c, 9)) return;
+    int n_samp = -1;
+    if (p.temperature > 0.f) n_samp = sample_verify_step();
     if (c.cta == 0) {
         int *am = reinterpret_cast<int *>(c.sm + SM_SCRATCH + 8192);
         if (c.tid < c.T) {
@@ -2601,6 +2790,7 @@ __device__ __noinline__ void consumer() {
                 if (__ldg(p.tokens + i) == am[i - 1]) n = i;
                 else break;
             }
+            if (n_samp >= 0) n = n_samp;
             *p.out_accepted = n;
             Ctrl *k = c.ctrl;
             k->steps += 1;

@@ -18,11 +18,12 @@ LIB_PATH = os.path.join(HERE, "libmk.so")
 MK_OK, MK_ERR_INVALID, MK_ERR_UNSUPPORTED, MK_ERR_NOMEM = 0, -1, -2, -3
 MK_ERR_TIMEOUT, MK_ERR_CUDA, MK_ERR_BAD_STATE, MK_ERR_BAD_INPUT, MK_ERR_RANGE = -4, -5, -6, -7, -8
 MK_DT_F32, MK_DT_BF16, MK_DT_FP8E4M3_B128, MK_DT_MXFP4_B32, MK_DT_FP8E4M3 = 0, 1, 2, 3, 4
-MK_DESC_VERSION = 2
+MK_DESC_VERSION = 3
 
 #: every symbol include/mk.h declares
-EXPORTS = ["mk_create", "mk_decode_step", "mk_decode_batch", "mk_decode_step_host", "mk_layer_forward",
-           "mk_get_status", "mk_get_stats", "mk_debug_skip_barrier", "mk_set_routing_trace", "mk_set_stage_trace", "mk_reset", "mk_layer_forward_noalloc", "mk_destroy", "mk_status_string",
+EXPORTS = ["mk_create", "mk_decode_step", "mk_decode_step_sample", "mk_decode_batch", "mk_decode_step_host",
+           "mk_layer_forward", "mk_get_status", "mk_get_stats", "mk_debug_skip_barrier", "mk_set_routing_trace",
+           "mk_set_stage_trace", "mk_reset", "mk_layer_forward_noalloc", "mk_destroy", "mk_status_string",
            "mk_last_error"]
 
 _vp = ctypes.c_void_p
@@ -39,7 +40,8 @@ class mk_model_desc(ctypes.Structure):
                 ("page_size", ctypes.c_int), ("max_T", ctypes.c_int),
                 ("max_pages_per_stream", ctypes.c_int), ("weight_dtype", ctypes.c_int),
                 ("router_dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int),
-                ("timeout_ms", ctypes.c_int), ("expert_dtype", ctypes.c_int)]
+                ("timeout_ms", ctypes.c_int), ("expert_dtype", ctypes.c_int),
+                ("lm_head_dtype", ctypes.c_int)]
 
 
 class mk_layer_weights(ctypes.Structure):
@@ -51,7 +53,7 @@ class mk_layer_weights(ctypes.Structure):
 
 class mk_weights(ctypes.Structure):
     _fields_ = [("embed", _vp), ("final_norm", _vp), ("lm_head", _vp),
-                ("layers", ctypes.POINTER(mk_layer_weights))]
+                ("layers", ctypes.POINTER(mk_layer_weights)), ("lm_head_scale", _vp)]
 
 
 class mk_kv_cache(ctypes.Structure):
@@ -86,6 +88,9 @@ def lib() -> ctypes.CDLL:
     L.mk_decode_step.argtypes = [_vp, _vp, ctypes.c_int, _vp, ctypes.POINTER(mk_kv_cache), _vp,
                                  _vp, _vp, _vp]
     L.mk_decode_step.restype = S
+    L.mk_decode_step_sample.argtypes = [_vp, _vp, ctypes.c_int, _vp, ctypes.POINTER(mk_kv_cache),
+                                        ctypes.c_float, _vp, _vp, _vp, _vp, _vp]
+    L.mk_decode_step_sample.restype = S
     L.mk_decode_batch.argtypes = [_vp, ctypes.c_int, _vp, ctypes.c_int, _vp,
                                   ctypes.POINTER(mk_kv_cache), _vp, _vp, _vp, _vp]
     L.mk_decode_batch.restype = S
@@ -162,6 +167,14 @@ def mk_decode_step(st, draft_tokens, T, positions, kv: mk_kv_cache, out_logits, 
                    out_argmax=None, stream=None, check=True) -> int:
     s = lib().mk_decode_step(st, _ptr(draft_tokens), T, _ptr(positions), ctypes.byref(kv),
                              _ptr(out_logits), _ptr(out_accepted), _ptr(out_argmax), _ptr(stream))
+    return _check(st, s) if check else s
+
+
+def mk_decode_step_sample(st, draft_tokens, T, positions, kv: mk_kv_cache, temperature, uniforms,
+                          out_logits, out_accepted, out_token, stream=None, check=True) -> int:
+    s = lib().mk_decode_step_sample(st, _ptr(draft_tokens), T, _ptr(positions), ctypes.byref(kv),
+                                    float(temperature), _ptr(uniforms), _ptr(out_logits),
+                                    _ptr(out_accepted), _ptr(out_token), _ptr(stream))
     return _check(st, s) if check else s
 
 
@@ -248,7 +261,7 @@ class ModelArgs:
             cfg.expert_inter, cfg.vocab, cfg.page_size, max_T, max_pages, cfg.weight_dtype,
             cfg.router_dtype, MK_DT_FP8E4M3 if cfg.kv_dtype == MK_DT_FP8E4M3_B128 else cfg.kv_dtype,
             timeout_ms,
-            getattr(cfg, "routed_dtype", cfg.weight_dtype))
+            getattr(cfg, "routed_dtype", cfg.weight_dtype), getattr(cfg, "lm_dtype", MK_DT_BF16))
         n = cfg.n_layers
         self.layers = (mk_layer_weights * n)()
         for i, L in enumerate(model.layers):
@@ -271,7 +284,8 @@ class ModelArgs:
             mat("ws2", L.ws2)
         self.weights = mk_weights(_ptr(getattr(model, "embed", None)),
                                   _ptr(getattr(model, "final_norm", None)),
-                                  _ptr(getattr(model, "lm_head", None)), self.layers)
+                                  _ptr(getattr(model, "lm_head", None)), self.layers,
+                                  _ptr(getattr(model, "lm_head_scale", None)))
 
 
 class KVArgs:

@@ -11,7 +11,7 @@ standing in for the real checkpoint and prompts):
   * RMSNorm weights     1 (``gamma_jitter`` > 0 gives 1 + jitter*U(-1,1))
   * router bias         U(-0.1, 0.1) (0 for the tiny fp32 layer)
   * cached K/V entries  N(0, 1), stored in the cache dtype
-  * embedding rows      N(0, 1) (bf16); LM head N(0, 1/H) (bf16)
+  * embedding rows      N(0, 1) (bf16); LM head N(0, 1/H) (bf16, or FP8 1x128 as the matrices)
   * page table          a seeded permutation of physical pages
   * FP8 weights         per 1x128 block: scale = amax/448, code = RNE(w/scale)
   * MXFP4 expert weights per 1x32 block: E8M0 scale 2^(floor(log2 amax) - 2),
@@ -56,6 +56,7 @@ class Config:
     rope_base: float = 10000.0
     gamma_jitter: float = 0.0
     expert_dtype: int = -1         # routed-expert storage; -1: the same as weight_dtype
+    lm_dtype: int = WDT_BF16       # LM head storage: bf16 or FP8 (1x128 scales)
     kv_scales: tuple = (1.0, 1.0)  # FP8 KV cache: (K, V) scale of every layer (value = code * scale),
                                    # or a list of per-layer (K, V) pairs
 
@@ -262,7 +263,8 @@ class Model:
     layers: List[Layer]
     embed: Optional[torch.Tensor] = None      # bf16 [V][H]
     final_norm: Optional[torch.Tensor] = None
-    lm_head: Optional[torch.Tensor] = None    # bf16 [V][H]
+    lm_head: Optional[torch.Tensor] = None    # bf16 [V][H], or uint8 FP8 codes
+    lm_head_scale: Optional[torch.Tensor] = None  # FP8 LM head: fp32 [H/128][V]
 
 
 def _gamma(cfg, device, *names):
@@ -301,8 +303,12 @@ def make_model(cfg: Config, device) -> Model:
         m.embed = randn((cfg.vocab, cfg.hidden), 1.0, device, cfg.seed, "embed",
                         dtype=torch.bfloat16)
         m.final_norm = _gamma(cfg, device, "final_norm")
-        m.lm_head = randn((cfg.vocab, cfg.hidden), cfg.hidden ** -0.5, device, cfg.seed,
-                          "lm_head", dtype=torch.bfloat16)
+        if cfg.lm_dtype == WDT_FP8:
+            m.lm_head, m.lm_head_scale = quantize_fp8_blocks(
+                randn((cfg.vocab, cfg.hidden), cfg.hidden ** -0.5, device, cfg.seed, "lm_head"))
+        else:
+            m.lm_head = randn((cfg.vocab, cfg.hidden), cfg.hidden ** -0.5, device, cfg.seed,
+                              "lm_head", dtype=torch.bfloat16)
     return m
 
 

@@ -47,6 +47,7 @@ __all__ = [
     "Linear", "dequant", "linear", "rmsnorm", "rope", "sigmoid", "silu",
     "attention_gqa", "route", "swiglu", "LayerView", "layer_forward", "stack_forward",
     "accept_count", "tokens_per_second", "step_seconds_from", "argmax_lowest",
+    "softmax_t", "sample_index", "sample_verify",
 ]
 
 
@@ -483,6 +484,62 @@ def accept_count(tokens: Sequence[int], argmax: Sequence[int]) -> int:
         else:
             break
     return n
+
+
+def softmax_t(logits_row: np.ndarray, temperature: float) -> np.ndarray:
+    """Sampling distribution at temperature t > 0: p = exp(l / t) / sum exp(l / t),
+    in fp64 with the maximum subtracted first (top-p 1: no truncation).  Pinned."""
+    z = np.asarray(logits_row, dtype=np.float64) / float(temperature)
+    e = np.exp(z - np.max(z))
+    return e / e.sum()
+
+
+def sample_index(weights: np.ndarray, v: float) -> int:
+    """Inverse-CDF draw in index order from non-negative weights: the smallest x
+    with w_0 + ... + w_x > v * sum(w), for a uniform v in [0, 1).  A zero weight
+    is never drawn.  Pinned (boundaries by hand)."""
+    w = np.asarray(weights, dtype=np.float64)
+    cum = np.cumsum(w)
+    target = float(v) * cum[-1]
+    x = int(np.searchsorted(cum, target, side="right"))
+    if x >= len(w):                       # v * sum at the very top: the last nonzero weight
+        x = int(np.nonzero(w > 0)[0][-1])
+    return x
+
+
+def sample_verify(logits: np.ndarray, tokens: Sequence[int], temperature: float,
+                  uniforms: Sequence[float]):
+    """Verification of a draft block by sampling at temperature t (top-p 1).
+
+    tokens = [d_0, d_1, ..., d_k]; row i of logits is the model's distribution
+    p_i = softmax_t(logits[i], t) after d_0..d_i.  The drafts are proposed
+    greedily, so the draft distribution at each position is a point mass on
+    d_i.  Speculative sampling then accepts d_i with probability
+    min(1, p_{i-1}(d_i) / 1) = p_{i-1}(d_i): draft i is accepted while every
+    earlier draft was and uniforms[i-1] < p_{i-1}(d_i).  With n drafts accepted,
+    the step emits d_1..d_n and one token drawn with uniforms[k]:
+      - after a rejection (n < k) from the residual max(0, p_n - q) normalised,
+        which for the point mass q on d_{n+1} is p_n with d_{n+1} removed;
+      - after k acceptances from p_k.
+    The emitted tokens are then distributed as sampling from the model one
+    token at a time.  Returns (n, drawn token).
+    (ezolabs "Appendix: method", Decode speed: temperature 1.0, top-p 1.0;
+    block verification, section "How we got here".)  Pinned.
+    """
+    lg = np.asarray(logits, dtype=np.float64)
+    k = len(tokens) - 1
+    n = 0
+    for i in range(1, k + 1):
+        p = softmax_t(lg[i - 1], temperature)
+        if float(uniforms[i - 1]) < p[int(tokens[i])]:
+            n = i
+        else:
+            break
+    p = softmax_t(lg[n], temperature)
+    if n < k:
+        p = p.copy()
+        p[int(tokens[n + 1])] = 0.0
+    return n, sample_index(p, float(uniforms[k]))
 
 
 def tokens_per_second(tokens_per_step: float, step_seconds: float) -> float:

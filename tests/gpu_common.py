@@ -69,6 +69,21 @@ class Built:
         return logits, int(acc.item()), am, tr
 
 
+    def step_sample(self, tokens, temperature, uniforms):
+        """mk_decode_step_sample: (accepted, drawn token, logits as numpy)."""
+        T = len(tokens)
+        tok = torch.tensor(tokens, dtype=torch.int32, device="cuda")
+        u = torch.tensor(np.asarray(uniforms, dtype=np.float32), device="cuda")
+        logits = torch.empty((T, self.cfg.vocab), dtype=torch.float32, device="cuda")
+        acc = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        out = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        mk.mk_decode_step_sample(self.st, tok, T, self.positions(T), self.kvargs.kv, temperature, u,
+                                 logits, acc, out)
+        st = mk.mk_get_status(self.st)
+        assert st == mk.MK_OK, mk.mk_last_error(self.st)
+        return int(acc.item()), int(out.item()), logits.cpu().numpy()
+
+
 def kth_gap(key_row, K):
     s = np.sort(key_row)[::-1]
     return s[K - 1] - s[K] if len(s) > K else np.inf

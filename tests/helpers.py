@@ -56,6 +56,8 @@ def embed_fn(model):
 
 
 def lm_head_lin(model):
+    if model.lm_head_scale is not None:
+        return oracle.Linear("fp8", synth._np(model.lm_head), synth._np(model.lm_head_scale))
     return oracle.Linear("bf16", synth._np(model.lm_head))
 
 

@@ -95,3 +95,14 @@ def test_fp8_kv_workload_bytes_and_name():
     w = bench.workload_of(f8)
     assert "ctx 65536" in w and "FP8 e4m3 KV (per-layer K/V scales 0.0125/0.0125)" in w
     assert bench.workload_of(synth.stack_config()) == bench.WORKLOAD
+
+
+def test_fp8_lm_head_bytes_and_name():
+    # FP8 LM head: one byte per weight plus a float32 scale per 128 inputs of a row
+    from latency_moe_decode_persistent_gb300 import synth
+    b16 = synth.stack_config()
+    f8 = synth.stack_config(lm_dtype=synth.WDT_FP8)
+    d = 1874
+    V, H = 129280, 4096
+    assert bench.algorithmic_bytes(b16, d, 2048) - bench.algorithmic_bytes(f8, d, 2048) == V * H * 2 - (V * H + 32 * V * 4)
+    assert "FP8 e4m3 1x128 LM head" in bench.workload_of(f8)

@@ -114,6 +114,66 @@ def test_mini_stack_fp8_kv_cache():
         b.close()
 
 
+def test_mini_stack_fp8_lm_head():
+    """FP8 E4M3 LM head with 1x128 scales: logits, argmax and accept count against
+    the oracle's exact decoding of the same codes."""
+    cfg = mini_stack(lm_dtype=synth.WDT_FP8, seed=26)
+    b = gc.Built(cfg)
+    try:
+        toks = make_drafts(b, 36, cfg.T - 1, 0.83, seed=8)
+        err, acc, r, log = compare_step(b, toks)
+        assert err < gc.TOL[synth.WDT_FP8], err
+    finally:
+        b.close()
+
+
+def _sampling_near_boundary(lg, toks, temp, u, n_ref, tok_ref, eps=1e-5):
+    """True when an accept test or the draw lies within eps of its decision
+    boundary (in the fp64 reading of the same logits), where float32 may decide
+    the other way."""
+    for i in range(1, min(n_ref + 2, len(toks))):
+        p = oracle.softmax_t(lg[i - 1], temp)
+        if abs(float(u[i - 1]) - p[int(toks[i])]) < eps:
+            return True
+    p = oracle.softmax_t(lg[n_ref], temp)
+    if n_ref < len(toks) - 1:
+        p[int(toks[n_ref + 1])] = 0.0
+    cum = np.cumsum(p) / p.sum()
+    v = float(u[-1])
+    lo = cum[tok_ref - 1] if tok_ref > 0 else 0.0
+    return abs(v - lo) < eps or abs(cum[tok_ref] - v) < eps
+
+
+@pytest.mark.parametrize("temp", [1.0, 0.6])
+def test_mini_stack_sampling_verify(temp):
+    """mk_decode_step_sample against the oracle's sampling rule applied to the
+    GPU's own logits (the logits themselves are compared with the oracle by the
+    argmax-path tests); decisions within 1e-5 of a boundary are skipped.  Then a
+    temperature of 1e-3 must reproduce argmax verification."""
+    cfg = mini_stack(seed=27)
+    b = gc.Built(cfg)
+    try:
+        rng = np.random.default_rng(12)
+        compared = 0
+        for trial in range(10):
+            toks = make_drafts(b, int(rng.integers(cfg.vocab)), cfg.T - 1, 0.83, seed=100 + trial)
+            u = rng.uniform(size=cfg.T).astype(np.float32)
+            n, tok, lg = b.step_sample(toks, temp, u)
+            lg64 = lg.astype(np.float64)
+            n_ref, tok_ref = oracle.sample_verify(lg64, toks, temp, u.astype(np.float64))
+            if _sampling_near_boundary(lg64, toks, temp, u, n_ref, tok_ref):
+                continue
+            assert (n, tok) == (n_ref, tok_ref), (trial, n, tok, n_ref, tok_ref)
+            compared += 1
+        assert compared >= 8
+        toks = make_drafts(b, 7, cfg.T - 1, 0.83, seed=5)
+        _, acc, am, _ = b.step(toks, trace=False)
+        n, tok, _ = b.step_sample(toks, 1e-3, np.full(cfg.T, 0.5, dtype=np.float32))
+        assert n == acc and tok == int(am[acc].item())
+    finally:
+        b.close()
+
+
 def test_mini_stack_all_drafts_accepted_and_deterministic():
     cfg = mini_stack(seed=31)
     b = gc.Built(cfg)
@@ -159,13 +219,27 @@ def test_full_43_layer_stack():
         b.close()
 
 
-def test_block_verification_is_batch_invariant():
+def _full_width_stack(**kw):
+    """3 layers of the 43-layer stack's full layer shape (H 4096, 384 experts
+    top-8, I 512), vocab 4096: the routed stages then hold several hundred
+    items per input chunk, more than the CTAs of a chunk, so the work split
+    puts both halves of some items on one CTA and splits others."""
+    c = synth.Config("full_width_3layer", 4096, 32, 4, 128, 384, 8, 512, n_layers=3, vocab=4096,
+                     weight_dtype=synth.WDT_FP8, router_dtype=synth.WDT_BF16,
+                     kv_dtype=synth.WDT_BF16, T=8, ctx=300, seed=52)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("make_cfg", [lambda: mini_stack(seed=51), _full_width_stack])
+def test_block_verification_is_batch_invariant(make_cfg):
     """Block verification = sequential decode, bit for bit on the GPU: the logits
     of position i from a step over the first i+1 tokens equal row i of the full
     step (the work split of the routed-expert stages changes with the set of
     distinct experts, so this pins that a token's result does not depend on the
     other tokens of the block).  The pages' greedy byte-for-byte gate, adapted."""
-    cfg = mini_stack(seed=51)
+    cfg = make_cfg()
     b = gc.Built(cfg)
     try:
         toks = [int(v) for v in np.random.default_rng(9).integers(0, cfg.vocab, cfg.T)]

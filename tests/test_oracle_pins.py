@@ -558,3 +558,79 @@ def test_stack_appended_identity_layer_changes_nothing():
     two_ident = _stack(model, cfg, toks)
     assert np.allclose(two_ident["logits"], one["logits"], rtol=1e-13, atol=1e-13)
     assert not np.allclose(two_live["logits"], one["logits"], rtol=1e-6, atol=1e-6)
+
+
+# ---------------------------------------------------------------------------
+# Temperature-sampling verification
+
+def test_softmax_t_closed_form():
+    # logits ln 1, ln 2, ln 3 at t = 1 give 1/6, 2/6, 3/6; at t = 1/2 the squares 1, 4, 9
+    l = np.log([1.0, 2.0, 3.0])
+    assert np.allclose(oracle.softmax_t(l, 1.0), [1 / 6, 2 / 6, 3 / 6], rtol=0, atol=1e-15)
+    assert np.allclose(oracle.softmax_t(l, 0.5), [1 / 14, 4 / 14, 9 / 14], rtol=0, atol=1e-15)
+    # a shift of every logit changes nothing (up to the rounding of l + 1000, an
+    # ulp of 1.1e-13); huge logits do not overflow
+    assert np.allclose(oracle.softmax_t(l + 1000.0, 1.0), [1 / 6, 2 / 6, 3 / 6], rtol=0, atol=1e-12)
+
+
+def test_sample_index_boundaries():
+    w = [1.0, 2.0, 3.0, 0.0]          # cumulative 1, 3, 6, 6 of 6
+    assert oracle.sample_index(w, 0.0) == 0
+    assert oracle.sample_index(w, 1 / 6 - 1e-9) == 0
+    assert oracle.sample_index(w, 1 / 6) == 1          # strictly above the cumulative 1
+    assert oracle.sample_index(w, 0.5 - 1e-9) == 1
+    assert oracle.sample_index(w, 0.5) == 2
+    assert oracle.sample_index(w, 1 - 1e-12) == 2      # the zero weight is never drawn
+    assert oracle.sample_index([0.0, 0.0, 5.0], 0.0) == 2
+
+
+def test_sample_verify_hand_case():
+    # t = 1, rows over 3 tokens with p = (1/6, 2/6, 3/6), (1/2, 1/4, 1/4), (0.1, 0.1, 0.8)
+    lg = np.log(np.array([[1, 2, 3], [2, 1, 1], [1, 1, 8]], dtype=np.float64))
+    # d_1 = 2: p_0(2) = 0.5 > 0.4 accepted; d_2 = 1: p_1(1) = 0.25 <= 0.3 rejected.
+    # Residual of row 1 without token 1: (1/2, 0, 1/4) / (3/4) = (2/3, 0, 1/3); v = 0.7 -> token 2
+    assert oracle.sample_verify(lg, [0, 2, 1], 1.0, [0.4, 0.3, 0.7]) == (1, 2)
+    # v = 0.6 -> token 0 (cumulative 2/3 > 0.6)
+    assert oracle.sample_verify(lg, [0, 2, 1], 1.0, [0.4, 0.3, 0.6]) == (1, 0)
+    # both accepted (0.4 < 0.5, 0.2 < 0.25): the bonus comes from row 2, v = 0.15 -> token 1
+    assert oracle.sample_verify(lg, [0, 2, 1], 1.0, [0.4, 0.2, 0.15]) == (2, 1)
+    # first draft rejected (0.5 is not < 0.5): residual of row 0 without token 2 is (1/3, 2/3, 0)
+    assert oracle.sample_verify(lg, [0, 2, 1], 1.0, [0.5, 0.0, 0.5]) == (0, 1)
+
+
+def test_sample_verify_emits_the_model_distribution():
+    # Speculative sampling's guarantee: the first emitted token (the draft if
+    # accepted, else the residual draw) is distributed as p_0, whatever the
+    # draft.  Integrate over a midpoint grid of (accept, draw) uniforms; the
+    # grid is exact to 1/N in each coordinate.
+    rng = np.random.default_rng(9)
+    V, N = 5, 300
+    lg = rng.normal(size=(2, V))
+    p0 = oracle.softmax_t(lg[0], 0.8)
+    grid = (np.arange(N) + 0.5) / N
+    for d in (0, 3):
+        counts = np.zeros(V)
+        for u in grid:
+            for v in grid:
+                n, tok = oracle.sample_verify(lg, [4, d], 0.8, [u, v])
+                counts[d if n == 1 else tok] += 1
+        assert np.max(np.abs(counts / N ** 2 - p0)) < 2.0 / N
+
+
+def test_sample_verify_low_temperature_is_greedy():
+    rng = np.random.default_rng(10)
+    V, T = 50, 6
+    for trial in range(20):
+        lg = rng.normal(size=(T, V))
+        am = oracle.argmax_lowest(lg)
+        toks = [int(rng.integers(V))]
+        for i in range(T - 1):
+            toks.append(int(am[i]) if rng.random() < 0.7 else int(rng.integers(V)))
+        u = rng.uniform(0.01, 0.99, size=T)
+        n, tok = oracle.sample_verify(lg, toks, 1e-4, u)
+        assert n == oracle.accept_count(toks, am)
+        if n < T - 1:
+            # the rejected draft differs from the argmax, which the residual then draws
+            assert tok == int(am[n])
+        else:
+            assert tok == int(am[T - 1])
