@@ -2112,7 +2112,12 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     unsigned char *scr = c.sm + SM_SCRATCH;
     float *part = m.att_part + (long long)(u.g * MK_MAXSPLIT + u.s) * MK_MAXROWS * D2;
     if (u.active && mma_path) {
-        const int nmt = (R + 15) / 16, nws = MK_NCWARPS / nmt;
+        // m-tiles of this launch's rows; the warp streams per m-tile follow the
+        // largest block the state takes, not this launch's T, so that a row's
+        // pages are summed and merged in the same order whatever the block
+        // size (batch invariance at long contexts, where a split holds
+        // several pages)
+        const int nmt = (R + 15) / 16, nws = MK_NCWARPS / max(nmt, (G * m.maxT + 15) / 16);
         const int mt = c.warp % nmt, ws = c.warp / nmt;
         const bool wact = c.warp < nmt * nws;
         AttMma A;

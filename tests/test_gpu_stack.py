@@ -222,8 +222,8 @@ def test_full_43_layer_stack():
 def _full_width_stack(**kw):
     """3 layers of the 43-layer stack's full layer shape (H 4096, 384 experts
     top-8, I 512), vocab 4096: the routed stages then hold several hundred
-    items per input chunk, more than the CTAs of a chunk, so the work split
-    puts both halves of some items on one CTA and splits others."""
+    items per input chunk, more than the CTAs of a chunk.  At ctx 8192 each
+    attention split holds several KV pages, which the warps of a split share."""
     c = synth.Config("full_width_3layer", 4096, 32, 4, 128, 384, 8, 512, n_layers=3, vocab=4096,
                      weight_dtype=synth.WDT_FP8, router_dtype=synth.WDT_BF16,
                      kv_dtype=synth.WDT_BF16, T=8, ctx=300, seed=52)
@@ -232,7 +232,8 @@ def _full_width_stack(**kw):
     return c
 
 
-@pytest.mark.parametrize("make_cfg", [lambda: mini_stack(seed=51), _full_width_stack])
+@pytest.mark.parametrize("make_cfg", [lambda: mini_stack(seed=51), _full_width_stack,
+                                      lambda: _full_width_stack(ctx=8192, seed=53)])
 def test_block_verification_is_batch_invariant(make_cfg):
     """Block verification = sequential decode, bit for bit on the GPU: the logits
     of position i from a step over the first i+1 tokens equal row i of the full
