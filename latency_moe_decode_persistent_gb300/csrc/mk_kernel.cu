@@ -1593,15 +1593,14 @@ __device__ __noinline__ void route_layer(const DLayer *Lp, RouteSm *rt) {
         for (int i = 0; i < 8; ++i)
             if (i == c.lane) mine = v[i];
         const int e = 511 - (int)(mine & 0x1ffu);
+        // the unbiased score of lane j's expert e: register e >> 5 of lane e & 31,
+        // fetched with one shuffle per register index
         float s = 0.f;
-        for (int j = 0; j < m.K; ++j) {
-            const int ej = __shfl_sync(0xffffffffu, e, j);
-            float val = 0.f;
+        const int src = e & 31, hi = e >> 5;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (i == (ej >> 5)) val = sg[i];
-            val = __shfl_sync(0xffffffffu, val, ej & 31);
-            if (c.lane == j) s = val;
+        for (int i = 0; i < 16; ++i) {
+            const float val = __shfl_sync(0xffffffffu, sg[i], src);
+            if (i == hi) s = val;
         }
         float sum = c.lane < m.K ? s : 0.f;
 #pragma unroll
