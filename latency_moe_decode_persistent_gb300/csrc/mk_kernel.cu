@@ -1821,10 +1821,10 @@ struct AttMma {
 // [2 boxes][nkeys][128 B] swizzled with box stride bs.  Keys are taken in
 // 32-key halves, each with its own online-softmax update.
 __device__ __forceinline__ void att_page_mma(const Ctx &c, AttMma &A, uint32_t kbase, uint32_t vbase, int bs,
-                             int nkeys, int valid, bool causal, int mt, int G) {
+                             int k0, int nkeys, int valid, bool causal, int mt, int G) {
     const int r = c.lane >> 2, q = c.lane & 3, mi = c.lane >> 3, li = c.lane & 7;
     const float sl2 = rsqrtf((float)c.m->d) * 1.4426950408889634f;
-    for (int h0 = 0; h0 < nkeys; h0 += 32) {
+    for (int h0 = k0; h0 < nkeys; h0 += 32) {
         const int nnt = min(4, (nkeys - h0) >> 3);
         float sc[4][4];
 #pragma unroll
@@ -1925,10 +1925,10 @@ __device__ __forceinline__ void att_page_mma(const Ctx &c, AttMma &A, uint32_t k
 // chunks of its key row per 32-key half.  PV: output column n of n-tile
 // 4g + np is physical head dim 32g + 4n + np, so a lane builds its B fragments
 // from one 4-byte word (4 dims) of each of its four key rows.
-__device__ __forceinline__ void att_page_fp8(const Ctx &c, AttMma &A, uint32_t kbase, uint32_t vbase, int nkeys, int valid,
-                             bool causal, int mt, int G, float sl2) {
+__device__ __forceinline__ void att_page_fp8(const Ctx &c, AttMma &A, uint32_t kbase, uint32_t vbase, int k0, int nkeys,
+                             int valid, bool causal, int mt, int G, float sl2) {
     const int r = c.lane >> 2, q = c.lane & 3;
-    for (int h0 = 0; h0 < nkeys; h0 += 32) {
+    for (int h0 = k0; h0 < nkeys; h0 += 32) {
         const int nnt = min(4, (nkeys - h0) >> 3);
         float sc[4][4];
         uint4 kw[4][2];
@@ -2128,23 +2128,27 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
             int row = mt * 16 + (c.lane & 7) + ((c.lane >> 3) & 1) * 8;
             A.qaddr = sa(scr) + row * 272 + (c.lane >> 4) * 16;
         }
+        // work units are 32-key halves of pages, dealt round-robin to the warp
+        // streams: with one page per split both halves run side by side
         for (int j = u.p0; j < u.pc1; ++j) {
             const int ks = ci % MK_RING;
             bool ok = mbar_wait(&c.full[ks], (ci / MK_RING) & 1, c, 210);
-            if (ok && wact && ((j - u.p0) % nws) == ws) {
-                int valid = min(m.P, c.ctx - j * m.P);
-                const uint32_t kb = sa(c.sm + SM_RING + ks * MK_SLOT);
-                if constexpr (fp8kv) att_page_fp8(c, A, kb, kb + MK_SLOT / 2, 64, valid, false, mt, G, sl2);
-                else att_page_mma(c, A, kb, kb + MK_SLOT / 2, bs, 64, valid, false, mt, G);
+            const int valid = min(m.P, c.ctx - j * m.P);
+            for (int h = 0; h < 2; ++h) {
+                if (ok && wact && ((j - u.p0) * 2 + h) % nws == ws && 32 * h < valid) {
+                    const uint32_t kb = sa(c.sm + SM_RING + ks * MK_SLOT);
+                    if constexpr (fp8kv) att_page_fp8(c, A, kb, kb + MK_SLOT / 2, 32 * h, 32 * h + 32, valid, false, mt, G, sl2);
+                    else att_page_mma(c, A, kb, kb + MK_SLOT / 2, bs, 32 * h, 32 * h + 32, valid, false, mt, G);
+                }
             }
             __syncwarp();
             if (c.lane == 0) mbar_arrive(&c.empty[ks]);
             ci += 1;
         }
-        if (u.has_new && wact && ((u.pc1 - u.p0) % nws) == ws) {
+        if (u.has_new && wact && ((u.pc1 - u.p0) * 2) % nws == ws) {
             uint32_t mini = sa(scr + 17408);
-            if constexpr (fp8kv) att_page_fp8(c, A, mini, mini + 4096, 16, c.T, true, mt, G, sl2);
-            else att_page_mma(c, A, mini, mini + 4096, 2048, 16, c.T, true, mt, G);
+            if constexpr (fp8kv) att_page_fp8(c, A, mini, mini + 4096, 0, 16, c.T, true, mt, G, sl2);
+            else att_page_mma(c, A, mini, mini + 4096, 2048, 0, 16, c.T, true, mt, G);
         }
         // finish row sums
 #pragma unroll
