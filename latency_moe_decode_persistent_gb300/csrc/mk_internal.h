@@ -35,7 +35,7 @@
 #define SM_ROUTE_BYTES 4096
 #define SM_BAR (SM_ROUTE + SM_ROUTE_BYTES)
 #define SM_MISC (SM_BAR + 256)
-#define SM_MISC_BYTES 2048
+#define SM_MISC_BYTES 3072
 #define SM_TOTAL (SM_MISC + SM_MISC_BYTES)
 
 // stages of one layer, in stream order

@@ -296,12 +296,25 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int byte) {
 }
 
 // ------------------------------------------------------------------ CTA context
+// input blocks of this CTA's fragment builds, fixed for the launch: the QKV
+// stage's (and those it stores sum-of-squares partials for), the O
+// projection's, the router stage's (and its partials)
+enum { KBM_QKV = 0, KBM_QKV_SSQ, KBM_O, KBM_RT, KBM_RT_SSQ };
+// The integer state with which a CTA starts walking its tiles of one GEMV
+// stage (see StageIter): its tile count and the (expert slot, matrix, row
+// group, column piece) of its first tile.  Working it out takes a chain of
+// integer divisions; the stages whose split is fixed for the launch get it once
+// at launch, the routed stages once per layer while the routing is published.
+struct StageSeed {
+    int n, ex, mat, rg, kc, kc0, kcn, kcn_sh, n_rg, n_kc, nmat, nex, nd;
+};
 struct RouteSm {
     int nd;
     int dlist[MK_MAXD];
     signed char dslot[MK_MAXD][MK_MAXT];
     int idx[MK_MAXT][MK_MAXK];
     float w[MK_MAXT][MK_MAXK];
+    StageSeed seed[2];           // this CTA's routed gate/up and down stages
 };
 // CTA-uniform state in shared memory: the model block and the current/next
 // layer's descriptors are copied here so that no stage reads them from global
@@ -321,6 +334,8 @@ struct MiscSm {
     const Params *p;             // points at pc below
     DModel m;
     DLayer L[2];                 // descriptors of layers with parity 0 / 1
+    StageSeed seed[8];           // this CTA's split of the stages fixed for the launch, by stage
+    uint32_t kbm[5];             // 128-column input blocks of the fragment builds (see KBM_*)
     Params pc;                   // the launch parameters: generic loads from the
                                  // kernel's parameter space are slow, shared memory is not
 };
@@ -688,12 +703,79 @@ __device__ uint32_t ssq_owner_mask(const Ctx &c, int cols) {
     return (0xffu << (8 * c0)) & all;
 }
 
-__device__ void stage_iter(StageIter &it, const Ctx &c, int st, const DLayer &L, const RouteSm *rt) {
+// this CTA's split of stage st (nd: routed experts of the layer, for the
+// routed stages).  Every layer of a model has the same matrix shapes, so the
+// split of the non-routed stages holds for the whole launch.
+__device__ void stage_seed(StageSeed &sd, const Ctx &c, int st, const DLayer &L, int nd) {
+    const DModel &m = *c.m;
+    sd.nmat = 1;
+    sd.nex = 1;
+    sd.nd = 0;
+    if (st == ST_SHA) {
+        sd.nmat = 2;
+        sd.nex = m.nshared;
+    } else if (st == ST_EXPA) {
+        sd.nmat = 2;
+        sd.nex = nd;
+        sd.nd = nd;
+    } else if (st == ST_EXPB) {
+        sd.nd = nd;
+        sd.nex = nd + m.nshared;
+    }
+    const DMat &d0 = st == ST_QKV ? L.qkv : st == ST_O ? L.o : st == ST_ROUTER ? L.router :
+                     st == ST_LM ? m.lm : st == ST_SHA ? L.s1 : st == ST_EXPA ? L.w1 : L.w2;
+    sd.n_rg = d0.n_rg;
+    sd.n_kc = d0.n_kc;
+    sd.kcn = (chunk_major(st) && d0.cols % 1024 == 0) ? 1024 / d0.cpk : sd.n_kc;
+    if (st == ST_EXPB) {
+        // items (expert slot, 256-row group), whole items per CTA as below; the
+        // shared expert's items have its own number of column pieces (MXFP4
+        // routed experts: 256 columns a piece, an FP8 shared expert: 128)
+        const int kr = sd.kcn, ks = m.nshared ? L.s2.n_kc : kr, nrt = sd.nd * sd.n_rg;
+        sd.kcn_sh = ks;
+        int bi, ei;
+        split_range(sd.nex * sd.n_rg, c.G, c.cta, bi, ei);
+        sd.n = (min(ei, nrt) - min(bi, nrt)) * kr + (max(ei, nrt) - max(bi, nrt)) * ks;
+        sd.ex = bi / sd.n_rg;
+        sd.rg = bi - sd.ex * sd.n_rg;
+        sd.mat = 0;
+        sd.kc0 = sd.kc = 0;
+        if (sd.ex >= sd.nd) sd.kcn = ks;
+        return;
+    }
+    sd.kcn_sh = sd.kcn;
+    const int nch = sd.n_kc / sd.kcn;
+    const int per_mat = sd.n_rg * sd.kcn, per_ex = sd.nmat * per_mat, per_ch = sd.nex * per_ex;
+    int b, e;
+    if (st == ST_EXPA) {
+        // whole items only: an item's partial sum is then formed by one CTA in
+        // a fixed tile order whatever the number of routed experts, so the
+        // step's result for a token does not depend on the other tokens of
+        // the block (batch invariance); per-CTA counts differ by one item
+        split_range(nch * per_ch / sd.kcn, c.G, c.cta, b, e);
+        b *= sd.kcn;
+        e *= sd.kcn;
+    } else {
+        split_range(nch * per_ch, c.G, c.cta, b, e);
+    }
+    sd.n = e - b;
+    const int ch = per_ch ? b / per_ch : 0;
+    int r = b - ch * per_ch;
+    sd.ex = per_ex ? r / per_ex : 0;
+    r -= sd.ex * per_ex;
+    sd.mat = per_mat ? r / per_mat : 0;
+    r -= sd.mat * per_mat;
+    sd.rg = r / sd.kcn;
+    sd.kc0 = ch * sd.kcn;
+    sd.kc = sd.kc0 + (r - sd.rg * sd.kcn);
+}
+
+// start walking this CTA's tiles of stage st: the layer's matrix descriptors
+// and the split worked out beforehand (the launch's for the non-routed stages,
+// the layer's routing for the routed ones)
+__device__ __forceinline__ void stage_iter(StageIter &it, const Ctx &c, int st, const DLayer &L, const RouteSm *rt) {
     const DModel &m = *c.m;
     it.st = st;
-    it.nmat = 1;
-    it.nex = 1;
-    it.nd = 0;
     it.dlist = rt->dlist;
     switch (st) {
         case ST_QKV: it.m0 = mat_regs(L.qkv); break;
@@ -703,69 +785,30 @@ __device__ void stage_iter(StageIter &it, const Ctx &c, int st, const DLayer &L,
         case ST_SHA:
             it.m0 = mat_regs(L.s1);
             it.m1 = mat_regs(L.s3);
-            it.nmat = 2;
-            it.nex = m.nshared;
             break;
         case ST_EXPA:
             it.m0 = mat_regs(L.w1);
             it.m1 = mat_regs(L.w3);
-            it.nmat = 2;
-            it.nex = rt->nd;
-            it.nd = rt->nd;
             break;
         default:  // ST_EXPB
             it.m0 = mat_regs(L.w2);
             it.m1 = mat_regs(L.s2);
-            it.nd = rt->nd;
-            it.nex = rt->nd + m.nshared;
             break;
     }
-    const DMat &d0 = st == ST_QKV ? L.qkv : st == ST_O ? L.o : st == ST_ROUTER ? L.router :
-                     st == ST_LM ? m.lm : st == ST_SHA ? L.s1 : st == ST_EXPA ? L.w1 : L.w2;
-    it.n_rg = d0.n_rg;
-    it.n_kc = d0.n_kc;
-    it.kcn = (chunk_major(st) && d0.cols % 1024 == 0) ? 1024 / d0.cpk : it.n_kc;
-    if (st == ST_EXPB) {
-        // items (expert slot, 256-row group), whole items per CTA as below; the
-        // shared expert's items have its own number of column pieces (MXFP4
-        // routed experts: 256 columns a piece, an FP8 shared expert: 128)
-        const int kr = it.kcn, ks = m.nshared ? L.s2.n_kc : kr, nrt = it.nd * it.n_rg;
-        it.kcn_sh = ks;
-        int bi, ei;
-        split_range(it.nex * it.n_rg, c.G, c.cta, bi, ei);
-        it.n = (min(ei, nrt) - min(bi, nrt)) * kr + (max(ei, nrt) - max(bi, nrt)) * ks;
-        it.ex = bi / it.n_rg;
-        it.rg = bi - it.ex * it.n_rg;
-        it.mat = 0;
-        it.kc0 = it.kc = 0;
-        if (it.ex >= it.nd) it.kcn = ks;
-        return;
-    }
-    it.kcn_sh = it.kcn;
-    const int nch = it.n_kc / it.kcn;
-    const int per_mat = it.n_rg * it.kcn, per_ex = it.nmat * per_mat, per_ch = it.nex * per_ex;
-    int b, e;
-    if (st == ST_EXPA) {
-        // whole items only: an item's partial sum is then formed by one CTA in
-        // a fixed tile order whatever the number of routed experts, so the
-        // step's result for a token does not depend on the other tokens of
-        // the block (batch invariance); per-CTA counts differ by one item
-        split_range(nch * per_ch / it.kcn, c.G, c.cta, b, e);
-        b *= it.kcn;
-        e *= it.kcn;
-    } else {
-        split_range(nch * per_ch, c.G, c.cta, b, e);
-    }
-    it.n = e - b;
-    const int ch = per_ch ? b / per_ch : 0;
-    int r = b - ch * per_ch;
-    it.ex = per_ex ? r / per_ex : 0;
-    r -= it.ex * per_ex;
-    it.mat = per_mat ? r / per_mat : 0;
-    r -= it.mat * per_mat;
-    it.rg = r / it.kcn;
-    it.kc0 = ch * it.kcn;
-    it.kc = it.kc0 + (r - it.rg * it.kcn);
+    const StageSeed &sd = st == ST_EXPA ? rt->seed[0] : st == ST_EXPB ? rt->seed[1] : c.misc->seed[st];
+    it.n = sd.n;
+    it.ex = sd.ex;
+    it.mat = sd.mat;
+    it.rg = sd.rg;
+    it.kc = sd.kc;
+    it.kc0 = sd.kc0;
+    it.kcn = sd.kcn;
+    it.kcn_sh = sd.kcn_sh;
+    it.n_rg = sd.n_rg;
+    it.n_kc = sd.n_kc;
+    it.nmat = sd.nmat;
+    it.nex = sd.nex;
+    it.nd = sd.nd;
 }
 
 // ------------------------------------------------------------------ producer
@@ -1056,6 +1099,25 @@ __device__ uint32_t needed_kb(int b, int e, const DMat &d) {
         mask |= span << ((kc * d.cpk) / 128);
     }
     return mask;
+}
+
+// this CTA's input blocks of the fragment builds, for the launch (one thread)
+__device__ __noinline__ void launch_masks() {
+    const Ctx c = make_ctx();
+    const DModel &m = *c.m;
+    const DLayer &L = c.misc->L[0];
+    uint32_t *k = c.misc->kbm;
+    int b, e;
+    split_range(L.qkv.n_rg * L.qkv.n_kc, c.G, c.cta, b, e);
+    // the owners of the first row group's tiles cover every block once: they
+    // also store the blocks' sum-of-squares partials
+    const int nkc = L.qkv.n_kc;
+    k[KBM_QKV] = needed_kb(b, e, L.qkv);
+    k[KBM_QKV_SSQ] = b < nkc ? needed_kb(b, min(e, nkc), L.qkv) : 0u;
+    split_range(L.o.n_rg * L.o.n_kc, c.G, c.cta, b, e);
+    k[KBM_O] = needed_kb(b, e, L.o);
+    k[KBM_RT] = chunk_kb_mask(c, m.H);
+    k[KBM_RT_SSQ] = ssq_owner_mask(c, m.H);
 }
 
 // ------------------------------------------------------------------ GEMV tiles
@@ -1631,6 +1693,11 @@ __device__ __noinline__ void route_layer(const DLayer *Lp, RouteSm *rt) {
             }
         }
         if (c.lane == 31) rt->nd = pre;
+    } else if (c.warp <= 2) {
+        // meanwhile warps 1 and 2 work out this CTA's split of the routed
+        // gate/up and down stages, which the producer and the consumers read
+        const int nd = __reduce_add_sync(0xffffffffu, c.lane < 16 ? __popc(c.misc->emask[c.lane]) : 0);
+        if (c.lane == 0) stage_seed(rt->seed[c.warp - 1], c, c.warp == 1 ? ST_EXPA : ST_EXPB, L, nd);
     }
     bar_consumers();
     if (c.warp < c.T && c.lane < m.K) {
@@ -2556,16 +2623,11 @@ __device__ __noinline__ void consumer() {
         {
             mark(c, ST_QKV * 16 + 5);
             ActSrc a{m.res, nullptr, m.H, L.attn_norm};
-            int b, e;
-            split_range(stage_total(m, ST_QKV, L, rt), c.G, c.cta, b, e);
             if (f32path) {
                 build_act32(a, m.H);
                 ssq_block(c, 0);
             } else {
-                // the owners of the first row group's tiles cover every block
-                // once: they also store the blocks' sum-of-squares partials
-                const int nkc = L.qkv.n_kc;
-                build_frags(a, needed_kb(b, e, L.qkv), b < nkc ? needed_kb(b, min(e, nkc), L.qkv) : 0u, 0);
+                build_frags(a, c.misc->kbm[KBM_QKV], c.misc->kbm[KBM_QKV_SSQ], 0);
             }
             mark(c, ST_QKV * 16 + 6);
             bar_consumers();
@@ -2588,10 +2650,8 @@ __device__ __noinline__ void consumer() {
         {
             mark(c, ST_O * 16 + 5);
             ActSrc a{nullptr, m.o_buf, m.Hq * m.d, nullptr};
-            int b, e;
-            split_range(stage_total(m, ST_O, L, rt), c.G, c.cta, b, e);
             if (f32path) build_act32(a, m.Hq * m.d);
-            else build_frags(a, needed_kb(b, e, L.o));
+            else build_frags(a, c.misc->kbm[KBM_O]);
             mark(c, ST_O * 16 + 6);
             bar_consumers();
             mark(c, ST_O * 16 + 0);
@@ -2606,7 +2666,7 @@ __device__ __noinline__ void consumer() {
                 build_act32(a, m.H);
                 ssq_block(c, 1);
             } else {
-                build_frags(a, chunk_kb_mask(c, m.H), ssq_owner_mask(c, m.H), 1);
+                build_frags(a, c.misc->kbm[KBM_RT], c.misc->kbm[KBM_RT_SSQ], 1);
             }
             mark(c, ST_ROUTER * 16 + 6);
             bar_consumers();
@@ -2883,6 +2943,15 @@ __global__ void __launch_bounds__(MK_THREADS, 1) mk_step_kernel(const __grid_con
             atomicExch(&ctrl->abort, 1);
         }
         return;
+    }
+    {
+        // the launch's split of the non-routed stages, one stage per warp
+        const int st = threadIdx.x >> 5;
+        if ((threadIdx.x & 31) == 0 && (st == ST_QKV || st == ST_O || st == ST_ROUTER || st == ST_SHA ||
+                                        (st == ST_LM && p.mode == 0)))
+            stage_seed(misc->seed[st], make_ctx(), st, misc->L[0], 0);
+        if (threadIdx.x == 32) launch_masks();
+        __syncthreads();
     }
     if ((threadIdx.x >> 5) == MK_NCWARPS) {
         if ((threadIdx.x & 31) < MK_PLANES) producer();
