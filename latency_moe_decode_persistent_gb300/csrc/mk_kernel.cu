@@ -1720,13 +1720,18 @@ __device__ float qkv_val(const Ctx &c, int t, int col) {
 template <bool kFP8>
 __device__ __forceinline__ void att_prepare(const Ctx &c, int l, const AttUnit &u, bool mma_path) {
     const DModel &m = *c.m;
-    const int G = m.Hq / m.Hkv, R = G * c.T, hd = m.d / 2;
+    // head dim 128 on the tensor-core path, 64 in the all-fp32 build; rows
+    // divide by G through its 16-bit reciprocal (exact for rows below 1024)
+    constexpr int hd = kF32 ? 32 : 64;
+    const int G = m.Hq / m.Hkv, R = G * c.T;
+    const uint32_t ginv = (65536u + G - 1) / G;
     constexpr bool fp8kv = kFP8;
     bool qbad = false;
     unsigned char *scr = c.sm + SM_SCRATCH;
     const long long *qkv = acc_ptr(m, ACC_QKV, c.misc->par);
     // rotated queries: 4 consecutive pairs per item, two items per thread and batch
-    const int nk4 = hd / 4, nitem = R * nk4;
+    constexpr int nk4 = hd / 4;
+    const int nitem = R * nk4;
     longlong2 xa[2][2], xb[2][2];
     float4 ra[2][2];
     auto load = [&](int i0) {
@@ -1735,7 +1740,7 @@ __device__ __forceinline__ void att_prepare(const Ctx &c, int l, const AttUnit &
             int i = i0 + u4 * MK_NCWARPS * 32;
             if (i < nitem) {
                 int row = i / nk4, k = (i - row * nk4) * 4;
-                int t = row / G, h = u.g * G + (row - t * G);
+                int t = (int)(((uint32_t)row * ginv) >> 16), h = u.g * G + (row - t * G);
                 const long long *b = qkv + (long long)t * m.nqkv + h * m.d + k;
                 xa[u4][0] = __ldcg(reinterpret_cast<const longlong2 *>(b));
                 xa[u4][1] = __ldcg(reinterpret_cast<const longlong2 *>(b) + 1);
@@ -1765,7 +1770,7 @@ __device__ __forceinline__ void att_prepare(const Ctx &c, int l, const AttUnit &
             int i = i0 + u4 * MK_NCWARPS * 32;
             if (i >= nitem) break;
             int row = i / nk4, k = (i - row * nk4) * 4;
-            float inv = c.misc->inv_rms[0][row / G];
+            float inv = c.misc->inv_rms[0][((uint32_t)row * ginv) >> 16];
             float x1[4] = {from_fx(xa[u4][0].x), from_fx(xa[u4][0].y), from_fx(xa[u4][1].x), from_fx(xa[u4][1].y)};
             float x2[4] = {from_fx(xb[u4][0].x), from_fx(xb[u4][0].y), from_fx(xb[u4][1].x), from_fx(xb[u4][1].y)};
             float cs[8] = {ra[u4][0].x, ra[u4][0].y, ra[u4][0].z, ra[u4][0].w,
@@ -2383,7 +2388,8 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     // pair) and take half of the splits each, so that one batch of loads in
     // flight covers up to 2 * 19 splits; each lane folds its half with the
     // running maximum, then the two halves are folded by one shuffle
-    const int hp = m.d / 2;
+    constexpr int hp = kF32 ? 32 : 64;  // column pairs of a head (dim 64 / 128)
+    const uint32_t ginv = (65536u + G - 1) / G;
     const long long sstr = (long long)MK_MAXROWS * D2;
     for (int item = c.tid; item < nr * hp * 2; item += MK_NCWARPS * 32) {  // warp-uniform bound
         const int half = item & 1, grp = item >> 1;
@@ -2430,7 +2436,7 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
         if (half == 0) {
             const float Mn = fmaxf(M, Mo), a = exp2f(M - Mn), b = exp2f(Mo - Mn);
             const float il = 1.f / (lsum * a + lo * b);
-            const int row = r0 + rr, t = row / G, h = u.g * G + (row - t * G);
+            const int row = r0 + rr, t = (int)(((uint32_t)row * ginv) >> 16), h = u.g * G + (row - t * G);
             __stcg(reinterpret_cast<float2 *>(m.o_buf + (long long)t * m.Hq * m.d + h * m.d + 2 * dp),
                    make_float2((acc.x * a + ox * b) * il, (acc.y * a + oy * b) * il));
         }
