@@ -1461,7 +1461,10 @@ __device__ __noinline__ uint32_t cons_gemv(int st, const DLayer *Lp, const Route
             cmat = it.mat;
             crg = it.rg;
             if (st == ST_EXPB && it.ex != last_hex) {
-                bar_consumers();
+                // the first build needs no barrier before it: the grid barrier
+                // that opened the stage already follows every warp's last use
+                // of the fragment area
+                if (k > 0) bar_consumers();
                 build_h_frags(rt, it.ex, kF32);
                 bar_consumers();
                 last_hex = it.ex;
@@ -1625,7 +1628,8 @@ __device__ __noinline__ void route_layer(const DLayer *Lp, RouteSm *rt) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int e = c.lane + 32 * i;
-            sg[i] = 1.f / (1.f + expf(-from_fx(raw[i]) * inv));
+            sg[i] = 0.f;  // register rows past the last expert hold no score
+            if (32 * i < m.E) sg[i] = 1.f / (1.f + expf(-from_fx(raw[i]) * inv));
             v[i] = e < m.E ? key32(sg[i] + bias[i], e) : 0u;
         }
         bitonic16_desc(v);
