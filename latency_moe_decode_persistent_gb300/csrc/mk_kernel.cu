@@ -79,25 +79,10 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ void tma2d(void *dst, const CUtensorMap *map, int x, int y,
-                                      uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(sa(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(sa(bar))
-        : "memory");
-}
-__device__ __forceinline__ void tma3d(void *dst, const CUtensorMap *map, int x, int y, int z,
-                                      uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sa(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(z), "r"(sa(bar))
-        : "memory");
-}
-// the same copies with an L2 eviction-priority hint (streamed weights are read
-// once per step: evict them first so that activations, accumulators, tensor
-// maps and code stay resident in L2)
+// TMA tile and bulk copies into shared memory, completing on an mbarrier, with
+// an L2 eviction-priority hint (streamed weights are read once per step: evict
+// them first so that activations, accumulators, tensor maps and code stay
+// resident in L2)
 __device__ __forceinline__ uint64_t l2_evict_first() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -125,14 +110,6 @@ __device__ __forceinline__ void bulk_g2s_h(void *dst, const void *src, uint32_t 
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
             "r"(sa(dst)),
         "l"(src), "r"(bytes), "r"(sa(bar)), "l"(pol)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
-                                         uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(sa(dst)),
-        "l"(src), "r"(bytes), "r"(sa(bar))
         : "memory");
 }
 __device__ __forceinline__ void bar_consumers() {
@@ -578,18 +555,6 @@ __device__ __forceinline__ long long *acc_ptr(const DModel &m, int which, int pa
     return b + (par ? acc_elems(m, which) : 0);
 }
 
-__device__ int stage_total(const DModel &m, int st, const DLayer &L, const RouteSm *rt) {
-    switch (st) {
-        case ST_QKV: return L.qkv.n_rg * L.qkv.n_kc;
-        case ST_O: return L.o.n_rg * L.o.n_kc;
-        case ST_ROUTER: return L.router.n_rg * L.router.n_kc;
-        case ST_SHA: return m.nshared ? 2 * L.s1.n_rg * L.s1.n_kc : 0;
-        case ST_EXPA: return rt->nd * 2 * L.w1.n_rg * L.w1.n_kc;
-        case ST_EXPB: return rt->nd * L.w2.n_rg * L.w2.n_kc + (m.nshared ? L.s2.n_rg * L.s2.n_kc : 0);
-        case ST_LM: return m.lm.n_rg * m.lm.n_kc;
-    }
-    return 0;
-}
 
 
 // attention split of a unit (one kv head, a run of pages)
@@ -2176,7 +2141,7 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
     const AttUnit u = att_unit(c);
     const int G = m.Hq / m.Hkv, R = G * c.T;
     constexpr bool mma_path = !kF32;
-    const int nbox = (m.d * m.kv_es) / 128, bs = m.P * 128;
+    const int bs = m.P * 128;
     const int D2 = m.d + 2;
     constexpr bool fp8kv = mma_path && kFP8;
     const float ksc = fp8kv ? c.p->kv_scale[2 * l] : 1.f, vsc = fp8kv ? c.p->kv_scale[2 * l + 1] : 1.f;
@@ -2340,7 +2305,6 @@ __device__ __noinline__ long long cons_att(int l, uint32_t ci) {
         float *mrg = reinterpret_cast<float *>(scr);
         const int WS = 16 * m.d + 32, MO = 16 * m.d;
         float *w = mrg + c.warp * WS;
-        const int nd = m.d / 32;
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) {
             if (rr < R) {
