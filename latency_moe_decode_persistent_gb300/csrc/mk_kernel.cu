@@ -423,10 +423,11 @@ __device__ __forceinline__ uint32_t f16x2_bad(uint32_t w) {
 // nonzero unless |v| < 2^31 (NaN included)
 __device__ __forceinline__ uint32_t fx_bad(float v) { return !(fabsf(v) < 2147483648.0f); }
 
-// bounded wait on an mbarrier phase: first try inline, the rest out of line
-__device__ __noinline__ bool mbar_wait_slow(uint64_t *b, uint32_t parity, int where) {
-    const Ctx c = make_ctx();
-    uint64_t t0 = gtimer();
+// bounded wait on an mbarrier phase, spun inline (no call on the path whose
+// length depends on timing)
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, const Ctx &c, int where) {
+    if (mbar_try(b, parity)) return true;
+    const uint64_t t0 = gtimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try(b, parity)) return true;
         if ((it & 15) == 0) {
@@ -437,10 +438,6 @@ __device__ __noinline__ bool mbar_wait_slow(uint64_t *b, uint32_t parity, int wh
             }
         }
     }
-}
-__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, const Ctx &c, int where) {
-    (void)c;
-    return mbar_try(b, parity) || mbar_wait_slow(b, parity, where);
 }
 // bounded wait that ignores the abort flag (drain of copies in flight)
 __device__ void mbar_wait_drain(uint64_t *b, uint32_t parity, const Ctx &c) {
